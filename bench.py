@@ -1,0 +1,375 @@
+"""Benchmark of the LazyAttention hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of the workload:
+prefill of every request's query segment against its documents (TTFT), then
+the configured number of decode steps (append + attention) for every request.
+Inputs are synthetic (seeded), resident in HBM before the timed region; the L2
+is flushed before every step; per-phase times come from CUDA events on the
+launching stream.
+
+Reported: value = decode KV-read throughput (logical K+V bytes of every
+request's full context per decode step / decode time), plus prefill TFLOP/s
+(QK^T and PV MMA FLOPs only), TTFT, roofline fractions, the in-run
+materialising baseline (copy + eager RoPE into private pages, then the same
+kernels without rotation), an end-to-end number through host buffers and the
+fp64 oracle timed on a bounded sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "llama3_8b"
+METRIC = "decode KV-read GB/s & prefill TFLOP/s (fraction of GB300 peak); TTFT ms"
+UNIT = "GB/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def work_model(cfg):
+    """Algorithmic bytes / FLOPs of one step of cfg (all requests)."""
+    R, Hkv, Hq, D = cfg.n_requests, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
+    esz = 4 if cfg.dtype == "f32" else 2
+    L0, Lq = cfg.context_len, cfg.q_len
+    pairs = Lq * L0 + Lq * (Lq + 1) // 2              # visible (query, key) pairs per head
+    prefill_flops = 4.0 * D * pairs * Hq * R
+    dec_bytes = [2.0 * (L0 + Lq + t + 1) * Hkv * D * esz * R for t in range(cfg.decode_steps)]
+    return prefill_flops, dec_bytes
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sms.append(float(parts[0]))
+                    mx = float(parts[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def run_ours(args, rank, world):
+    import torch
+    import workload
+    import workload.device as wdev
+    import __graft_entry__
+    __graft_entry__.build()
+    import position_agnostic_kv_lazyattn_gb300 as L
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = workload.CONFIGS[args.config]
+    env = wdev.setup(cfg, baseline=True)
+    R = cfg.n_requests
+    b = env.batch
+    stream = torch.cuda.current_stream()
+    hbm_peak, tc_peak, tc_sust, peak_kind = peaks()
+    prefill_flops, dec_bytes = work_model(cfg)
+
+    # per-step inputs, resident in HBM
+    dec_in = [wdev.decode_step_tensors(cfg, t, range(R)) for t in range(cfg.decode_steps)]
+    out_p = torch.empty((max(b.total_q, 1), cfg.n_q_heads, cfg.head_dim), dtype=env.pool.tdtype, device=dev)
+    out_d = torch.empty((R, cfg.n_q_heads, cfg.head_dim), dtype=env.pool.tdtype, device=dev)
+    ws_bytes = L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_DECODE, b.c)
+    ws = torch.zeros((ws_bytes + 3) // 4, dtype=torch.int32, device=dev)
+    entries0 = b.entries.clone()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # > 129 MB L2
+
+    # materialising baseline: private copies of every entry's page
+    base_pages = env.pool.alloc_pages(len(b.entries_host))
+    dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.array(base_pages, np.uint64)
+    dst_dev = torch.from_numpy(dst.view(np.int64).copy()).to(dev)
+    mb = b.with_entries(dst, L.LAZYATTN_KEYS_PREROTATED, device=dev)
+    mb_entries0 = mb.entries.clone()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def lazy_step(rec):
+        b.entries.copy_(entries0)
+        flush.zero_()
+        e = [ev() for _ in range(cfg.decode_steps + 2)]
+        e[0].record(stream)
+        if b.total_q:
+            L.lazyattn_prefill(env.pool.handle, b.c, env.q, out_p, None, 0, stream)
+        e[1].record(stream)
+        for t in range(cfg.decode_steps):
+            q, k, v = dec_in[t]
+            L.lazyattn_decode(env.pool.handle, b.c, q, k, v, out_d, ws, ws_bytes, stream)
+            e[t + 2].record(stream)
+        rec.append(e)
+
+    def base_step(rec):
+        mb.entries.copy_(mb_entries0)
+        flush.zero_()
+        e = [ev() for _ in range(4)]
+        e[0].record(stream)
+        L.lazyattn_materialize(env.pool.handle, b.c, dst_dev, stream)
+        e[1].record(stream)
+        if b.total_q:
+            L.lazyattn_prefill(env.pool.handle, mb.c, env.q, out_p, None, 0, stream)
+        e[2].record(stream)
+        for t in range(cfg.decode_steps):
+            q, k, v = dec_in[t]
+            L.lazyattn_decode(env.pool.handle, mb.c, q, k, v, out_d, ws, ws_bytes, stream)
+        e[3].record(stream)
+        rec.append(e)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        lazy_step([])
+    barrier()
+    rec = []
+    with Clocks(dev.index) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            lazy_step(rec)
+        barrier()
+        wall = time.perf_counter() - t0
+    status = env.pool.device_status()
+
+    pre_ms = [r[0].elapsed_time(r[1]) for r in rec]
+    dec_ms = [r[1].elapsed_time(r[-1]) for r in rec]
+    dec_call_ms = [r[t + 1].elapsed_time(r[t + 2]) for r in rec for t in range(cfg.decode_steps)]
+    step_ms = [p + d for p, d in zip(pre_ms, dec_ms)]
+    dec_total_bytes = sum(dec_bytes)
+    mean_dec_s = statistics.mean(dec_ms) / 1e3
+    local = {"step_ms": statistics.mean(step_ms), "dec_s": mean_dec_s, "pre_ms": statistics.mean(pre_ms),
+             "wall": wall}
+    local = reduce_max_over_ranks(local, world)
+    if rank != 0:
+        return None
+
+    # baseline (same box, same inputs)
+    for _ in range(max(1, args.warmup // 2)):
+        base_step([])
+    torch.cuda.synchronize()
+    brec = []
+    for _ in range(max(1, min(args.steps, 3))):
+        base_step(brec)
+    torch.cuda.synchronize()
+    b_mat = statistics.mean(r[0].elapsed_time(r[1]) for r in brec)
+    b_pre = statistics.mean(r[1].elapsed_time(r[2]) for r in brec)
+    b_dec = statistics.mean(r[2].elapsed_time(r[3]) for r in brec)
+
+    # end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if cfg.decode_steps:
+        host_in = [tuple(x.cpu().pin_memory() for x in dec_in[t]) for t in range(cfg.decode_steps)]
+        host_out = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+        dq = torch.empty_like(dec_in[0][0]); dk = torch.empty_like(dec_in[0][1]); dv = torch.empty_like(dec_in[0][2])
+        h2d = sum(x.numel() * x.element_size() for x in host_in[0])
+        d2h = host_out.numel() * host_out.element_size()
+        times = []
+        for it in range(2):
+            b.entries.copy_(entries0)
+            flush.zero_()
+            torch.cuda.synchronize()
+            s0, s1 = ev(), ev()
+            s0.record(stream)
+            for t in range(cfg.decode_steps):
+                hq, hk, hv = host_in[t]
+                dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+                L.lazyattn_decode(env.pool.handle, b.c, dq, dk, dv, out_d, ws, ws_bytes, stream)
+                host_out.copy_(out_d, non_blocking=True)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            times.append(s0.elapsed_time(s1) / 1e3)
+        e2e = {"value": round(dec_total_bytes / min(times) / 1e9, 1), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "note": "decode phase with per-step pinned H2D of q/k_new/v_new and D2H of the output"}
+
+    dec_gbs = world * dec_total_bytes / local["dec_s"] / 1e9 if cfg.decode_steps else 0.0
+    pre_tflops = prefill_flops / (local["pre_ms"] / 1e3) / 1e12 if cfg.q_len else 0.0
+    mean_call = statistics.mean(dec_call_ms) if dec_call_ms else 0.0
+    per_call_bytes = dec_total_bytes / max(cfg.decode_steps, 1)
+    achieved = per_call_bytes / (mean_call / 1e3) / 1e9 if mean_call else 0.0
+    line = {
+        "metric": METRIC, "value": round(dec_gbs, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(local["step_ms"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": cfg.name, "requests": R, "docs_per_request": cfg.docs_per_request,
+                   "doc_len": cfg.doc_len, "pool_docs": cfg.n_docs, "q_heads": cfg.n_q_heads,
+                   "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "query_len": cfg.q_len,
+                   "decode_steps": cfg.decode_steps, "zipf_alpha": cfg.zipf_alpha, "seed": cfg.seed,
+                   "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}"},
+        "prefill_tflops": round(pre_tflops, 2), "ttft_ms": round(local["pre_ms"], 4),
+        "decode_ms_per_token_step": round(mean_call, 4),
+        "frac_hbm_peak": round(dec_gbs / world / hbm_peak, 4),
+        "frac_tensor_peak": round(pre_tflops / world / tc_peak, 4),
+        "roofline": {"kernel": "lazyattn_decode (append + split-K attention)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind},
+        "prefill_roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(pre_tflops, 2),
+                             "peak": tc_peak, "unit": "TFLOP/s", "frac": round(pre_tflops / tc_peak, 4),
+                             "peak_kind": peak_kind},
+        "materialising_baseline": {"materialise_ms": round(b_mat, 4), "ttft_ms": round(b_mat + b_pre, 4),
+                                   "decode_ms": round(b_dec, 4),
+                                   "decode_gbs": round(dec_total_bytes / (b_dec / 1e3) / 1e9, 1) if b_dec else None,
+                                   "lazy_ttft_speedup": round((b_mat + b_pre) / local["pre_ms"], 3),
+                                   "lazy_step_speedup": round((b_mat + b_pre + b_dec) / local["step_ms"], 3)},
+        "e2e": e2e,
+        "gpu_launches": args.steps * ((1 if cfg.q_len else 0) + 2 * cfg.decode_steps),
+        "wall_s_timed": round(local["wall"], 4),
+        "device_status": status,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
+    return line
+
+
+def reduce_max_over_ranks(local: dict, world: int) -> dict:
+    """Timing of a multi-rank run = the slowest rank (max over ranks)."""
+    if world <= 1:
+        return dict(local)
+    import torch
+    import torch.distributed as dist
+    keys = sorted(local)
+    t = torch.tensor([float(local[k]) for k in keys], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(keys, t.tolist()))
+
+
+def cpu_baseline(cfg, budget_s=15.0, n_steps=None):
+    """The fp64 oracle, as it stands, on a bounded sample: decode steps of a few
+    requests (every step attends over the request's full context)."""
+    import oracle
+    import workload
+    docs = workload.request_docs(cfg)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    esz = 4 if cfg.dtype == "f32" else 2
+    done_req = 0
+    steps = n_steps or min(cfg.decode_steps, 2) or 1
+    for r in range(cfg.n_requests):
+        ctx = [workload.doc_kv(cfg, int(d)) for d in docs[r]]
+        if cfg.q_len:
+            _, kq, vq = workload.query_segment(cfg, r)
+        else:
+            kq = np.zeros((0, cfg.n_kv_heads, cfg.head_dim), np.float32)
+            vq = kq.copy()
+        st = [tuple(a[0] for a in workload.decode_inputs(cfg, t, [r])) for t in range(steps)]
+        ts = time.perf_counter()
+        oracle.decode_request(ctx, kq, vq, st, cfg.rope_theta)
+        nbytes += sum(2.0 * (cfg.context_len + cfg.q_len + t + 1) * cfg.n_kv_heads * cfg.head_dim * esz
+                      for t in range(steps))
+        done_req += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(nbytes / el / 1e9, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done_req} request(s) x {steps} decode step(s) of {cfg.name}, fp64 numpy, "
+                      f"{el:.1f} s incl. input generation"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import workload
+    cfg = workload.CONFIGS[args.config]
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, budget_s=0.0, n_steps=1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(cfg, budget_s=0.0, n_steps=1))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "kind": "oracle", "cores": os.cpu_count(),
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend)
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * lazyattn.h - C ABI of a GB300 (sm_103a) implementation of LazyAttention's
+ * hot path: attention over a paged KV pool whose keys are stored WITHOUT rotary
+ * position encoding; RoPE is applied inside the prefill and decode kernels at
+ * each request's logical positions.
+ *
+ * Source: "LazyAttention: Efficient Retrieval-Augmented Generation with
+ * Deferred Positional Encoding".
+ *   - §3 "Problem statement": reuse a document's KV at any global offset, with
+ *     several requests of one batch reading one document at different offsets.
+ *   - §3.1 "Deferred encoding": Q, K, V are produced without positions; the cache
+ *     is content-only; positions are applied during attention.
+ *   - §3.1 Eq. 4: softmax(f(Q,m) f(K,n)^T / sqrt(d_k)) V, d_k = head_dim.
+ *   - §3.2 "Prefilling": rotation of the half-dimension pair (k[i], k[i+D/2]) by
+ *     angle a: k1' = k1 cos a - k2 sin a, k2' = k1 sin a + k2 cos a; cos/sin are
+ *     table-driven.
+ *   - §3.2 "Decoding": bit-packed 64-bit per-block metadata (block, offset, mask).
+ *   - §3.5 "GQA/MQA compatibility": query head h reads KV head h / (Hq/Hkv).
+ *   - Appendix C.4: angles from absolute indices m * theta_i.
+ *
+ * Conventions for every entry point
+ *   - Every device buffer (pools, position table, q/k/v/out, tables, workspace,
+ *     status word) is allocated and owned by the caller. The library never calls
+ *     cudaMalloc/cudaFree; it owns only host-side metadata (free-page list).
+ *   - Calls taking a stream enqueue work on it and return without synchronising,
+ *     except lazyattn_pool_create and lazyattn_get_device_status (documented).
+ *   - Argument errors are detected on the host, return a negative status and
+ *     launch nothing. Index errors found on the device (page id out of range,
+ *     position outside the table, no free decode slot) skip the offending work
+ *     and record the first error code in the caller's device status word; they
+ *     never trap or hang.
+ *   - Not thread-safe per pool: serialise calls that share a pool handle.
+ *
+ * Data layout in device memory (row-major, innermost last)
+ *   K pool, V pool : [num_pages][n_kv_heads][16][head_dim], element type dtype,
+ *                    pre-RoPE. A (page, kv-head) tile is contiguous.
+ *   position table : float2 [max_position][head_dim/2] = (cos, sin) of
+ *                    pos * theta^(-2i/head_dim), computed in fp64, stored fp32.
+ *   block table    : uint64 entries, see lazyattn_pack_entry.
+ */
+#ifndef LAZYATTN_H
+#define LAZYATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LAZYATTN_PAGE_SIZE 16
+#define LAZYATTN_MAX_START ((1 << 26) - 1)
+
+typedef enum lazyattn_status {
+    LAZYATTN_OK = 0,
+    LAZYATTN_EINVAL = -1,     /* bad argument: null pointer, inconsistent or unsupported size */
+    LAZYATTN_ENOSPC = -2,     /* not enough free pages in the pool */
+    LAZYATTN_ERANGE = -3,     /* page id or logical position outside the pool / table */
+    LAZYATTN_EDTYPE = -4,     /* dtype not supported by this entry point */
+    LAZYATTN_ECUDA = -5,      /* a CUDA runtime call or kernel launch failed */
+    LAZYATTN_EDEVICE = -6,    /* device-side check failed (see lazyattn_get_device_status) */
+    LAZYATTN_EWORKSPACE = -7, /* workspace smaller than lazyattn_workspace_size() */
+    LAZYATTN_ENODECODE = -8   /* device status only: a request had no writable free slot */
+} lazyattn_status;
+
+typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dtype;
+
+/* batch flags */
+#define LAZYATTN_KEYS_PREROTATED 1  /* K pages already hold RoPE at their logical positions
+                                       (the materialising baseline); kernels rotate q only */
+
+/* Pool description. All pointers are device pointers owned by the caller.
+ *   num_pages     pages in each of k_pool / v_pool (>= 1)
+ *   page_size     must be LAZYATTN_PAGE_SIZE (16)
+ *   n_q_heads     Hq; n_kv_heads Hkv; Hq % Hkv == 0
+ *   head_dim      D: 64 or 128 for LAZYATTN_F32; 128 for LAZYATTN_BF16
+ *   dtype         element type of the pools, q, k_new, v_new and out
+ *   rope_theta    RoPE base (> 0), frequencies theta^(-2i/D), i < D/2
+ *   max_position  the position table covers logical positions [0, max_position)
+ *   k_pool/v_pool [num_pages][n_kv_heads][16][head_dim]
+ *   rope_table    float2 [max_position][head_dim/2]; filled by lazyattn_pool_create
+ *   status_word   one int32 in device memory, zeroed by lazyattn_pool_create; kernels
+ *                 record the first device-side error there
+ */
+typedef struct lazyattn_pool_desc {
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t dtype;
+    double rope_theta;
+    int32_t max_position;
+    void* k_pool;
+    void* v_pool;
+    void* rope_table;
+    int32_t* status_word;
+} lazyattn_pool_desc;
+
+typedef struct lazyattn_pool* lazyattn_pool_t;
+
+/* A batch of requests. Device arrays unless stated otherwise.
+ *   num_requests   R >= 1 (host value)
+ *   max_entries    host upper bound on entries per request (grid sizing)
+ *   max_q_len      prefill: host upper bound on query tokens per request; decode: unused
+ *   total_q        prefill: number of rows of q / out (host value); decode: unused
+ *   entries        packed entries of all requests back to back; lazyattn_decode
+ *                  updates the entry it appends into, so this must be writable
+ *   entry_offsets  int32 [R+1]: request r owns entries [entry_offsets[r], entry_offsets[r+1])
+ *   q_offsets      prefill: int32 [R+1], request r owns rows [q_offsets[r], q_offsets[r+1]) of q/out
+ *   q_start        prefill: int32 [R], logical position of request r's first query row;
+ *                  row i of the request sits at q_start[r] + i
+ *   flags          0 or LAZYATTN_KEYS_PREROTATED
+ */
+typedef struct lazyattn_batch {
+    int32_t num_requests;
+    int32_t max_entries;
+    int32_t max_q_len;
+    int32_t total_q;
+    uint64_t* entries;
+    const int32_t* entry_offsets;
+    const int32_t* q_offsets;
+    const int32_t* q_start;
+    int32_t flags;
+} lazyattn_batch;
+
+#define LAZYATTN_OP_PREFILL 0
+#define LAZYATTN_OP_DECODE 1
+
+/* Human-readable name of a status code. Never NULL. */
+const char* lazyattn_status_string(int status);
+
+/* Pack one block-table entry (§3.2 "Decoding": block id, offset and mask in one
+ * 64-bit word). Field layout:
+ *   bits  0..31  physical page id
+ *   bits 32..57  logical position of slot 0 of the page (<= LAZYATTN_MAX_START)
+ *   bits 58..62  number of valid slots, 0..16 (slots [0, nvalid) hold tokens)
+ *   bit  63      writable: lazyattn_decode may append into this page
+ * Token at slot s of the page has logical position start + s. Out-of-range
+ * fields are masked to their width (host helper; no validation). */
+uint64_t lazyattn_pack_entry(int32_t page, int32_t start, int32_t nvalid, int32_t writable);
+
+/* Bytes of the position table for head_dim and max_position (host helper). */
+size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position);
+
+/* Create a pool over caller-owned buffers. Validates desc, fills the position
+ * table (fp64 on the host, stored fp32) and zeroes the status word on `stream`,
+ * then synchronises that stream before returning. All pages start free.
+ * Returns LAZYATTN_OK and *out_pool, or EINVAL/EDTYPE/ECUDA (nothing created). */
+int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_pool_t* out_pool);
+
+/* Release the host metadata of a pool (device buffers stay with the caller). */
+int lazyattn_pool_destroy(lazyattn_pool_t pool);
+
+/* Number of free pages (host). */
+int lazyattn_pool_free_count(lazyattn_pool_t pool, int32_t* out_count);
+
+/* Take n free pages (lowest ids first) for caller-managed contents, e.g. the
+ * private pages a request reserves for generated tokens. out_pages: host array
+ * of n ids. ENOSPC (nothing taken) if fewer than n are free. */
+int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages);
+
+/* Return pages to the free list. ERANGE for an id outside the pool, EINVAL for
+ * a page that is already free (nothing freed in either case). The caller must
+ * not free pages that queued kernels still read. */
+int lazyattn_free_pages(lazyattn_pool_t pool, const int32_t* pages, int32_t n);
+
+/* Store a document's (or a query segment's) pre-RoPE K/V in fresh pages.
+ * k, v: device [n_tokens][n_kv_heads][head_dim] in the pool dtype, unrotated.
+ * Allocates ceil(n_tokens/16) pages, enqueues the copy on `stream`, writes the
+ * page ids (in token order) to the host array out_pages (capacity out_cap) and
+ * their number to *out_npages. Page j holds tokens [16j, 16j+16); the caller
+ * builds entries (page_j, doc_start + 16j, nvalid_j, writable) from them.
+ * EINVAL if n_tokens < 1 or out_cap too small; ENOSPC if the pool is full. */
+int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32_t n_tokens,
+                       void* stream, int32_t* out_pages, int32_t out_cap, int32_t* out_npages);
+
+/* Bytes of workspace that lazyattn_prefill (op = LAZYATTN_OP_PREFILL) or
+ * lazyattn_decode (op = LAZYATTN_OP_DECODE) needs for this batch shape. The
+ * workspace is caller-allocated device memory, 256-byte aligned, and must be
+ * ZERO-FILLED before its first use; every completed call leaves the parts that
+ * must start at zero back at zero. Calls sharing one workspace must not
+ * overlap in time. Returns 0 on invalid arguments. */
+size_t lazyattn_workspace_size(lazyattn_pool_t pool, int32_t op, const lazyattn_batch* batch);
+
+/* Prefill attention (§3.2 "Prefilling"; §3.4 TTFT).
+ * q   : device [total_q][n_q_heads][head_dim], pre-RoPE, pool dtype.
+ * out : device [total_q][n_q_heads][head_dim], pool dtype, caller-allocated.
+ * Row i of request r (logical position m = q_start[r] + i), head h, reads KV head
+ * h / (Hq/Hkv) and attends over every token of the request's entries whose
+ * logical position n <= m, with q rotated at m and each key rotated at its own n
+ * (unless LAZYATTN_KEYS_PREROTATED), scale 1/sqrt(head_dim). The query
+ * segment's own K/V must already be stored and listed in the entries. Entries
+ * with nvalid = 0 contribute nothing. A row that sees no key gets zeros.
+ * Pool pages are only read. */
+int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q, void* out,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step for every request (§3.2 "Decoding"; §3.4 decoding latency).
+ * q     : device [R][n_q_heads][head_dim], pre-RoPE.
+ * k_new, v_new : device [R][n_kv_heads][head_dim], pre-RoPE K and V of the new token.
+ * out   : device [R][n_q_heads][head_dim].
+ * For request r the new token is appended into the first entry with nvalid < 16
+ * within the trailing run of writable entries of the request; it lands in slot
+ * nvalid of that page (logical position m = start + nvalid) and the entry's
+ * nvalid is incremented in place. Then q (rotated at m) attends over all the
+ * request's tokens, including the new one. With LAZYATTN_KEYS_PREROTATED the new
+ * key is stored rotated at m. If a request has no writable free slot its output
+ * is zeros and LAZYATTN_ENODECODE is recorded in the status word.
+ * Only the appended slot of a writable page is written; other pages are read. */
+int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q,
+                    const void* k_new, const void* v_new, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Materialising baseline (what re-encoding systems such as Block-Attention do,
+ * §4 "Baselines" and Appendix B): for every entry of `batch`, copy page
+ * src -> dst_entries[i].page, rotating K at the entry's logical positions (RoPE
+ * applied eagerly and stored in the pool dtype) and copying V unchanged. Entry
+ * i of dst_entries must carry the same start and nvalid as entry i of the batch
+ * and a distinct page per entry (its own private copy). dst_entries is a device
+ * array parallel to batch->entries. Run prefill/decode on the destination
+ * entries with LAZYATTN_KEYS_PREROTATED afterwards. */
+int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch,
+                         const uint64_t* dst_entries, void* stream);
+
+/* Debug view of block-table decoding: for every valid token of every request,
+ * in table order, write (page, slot, logical position) as three int32 to
+ * out_triples (device, capacity out_cap triples). Tokens of request r start at
+ * row out_offsets[r] (device int32 [R+1], exclusive prefix sum of valid-token
+ * counts, computed by the caller). Used to check indexing bit-exactly. */
+int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const int32_t* out_offsets,
+                     int32_t* out_triples, int32_t out_cap, void* stream);
+
+/* Copy the device status word to *out_status (synchronises `stream`), then
+ * reset it to zero if reset != 0. 0 means no device-side error since the last
+ * reset; otherwise a negative lazyattn_status. */
+int lazyattn_get_device_status(lazyattn_pool_t pool, int32_t* out_status, int32_t reset, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAZYATTN_H */

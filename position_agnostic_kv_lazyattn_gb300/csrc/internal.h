@@ -1,0 +1,106 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "lazyattn.h"
+
+namespace lazyattn {
+
+constexpr int kPage = LAZYATTN_PAGE_SIZE;
+
+// ---------------------------------------------------------------- entries
+// Field layout fixed by lazyattn_pack_entry (lazyattn.h).
+__host__ __device__ __forceinline__ uint32_t entry_page(uint64_t e) { return (uint32_t)(e & 0xffffffffull); }
+__host__ __device__ __forceinline__ int32_t entry_start(uint64_t e) { return (int32_t)((e >> 32) & ((1ull << 26) - 1)); }
+__host__ __device__ __forceinline__ int32_t entry_nvalid(uint64_t e) { return (int32_t)((e >> 58) & 0x1f); }
+__host__ __device__ __forceinline__ bool entry_writable(uint64_t e) { return (e >> 63) != 0; }
+__host__ __device__ __forceinline__ uint64_t make_entry(uint32_t page, int32_t start, int32_t nvalid, bool w) {
+    return (uint64_t)page | ((uint64_t)(start & ((1 << 26) - 1)) << 32) | ((uint64_t)(nvalid & 0x1f) << 58) |
+           ((uint64_t)(w ? 1 : 0) << 63);
+}
+
+// Shape and buffers a kernel needs about the pool (passed by value).
+struct PoolView {
+    void* k_pool;
+    void* v_pool;
+    const float2* rope;   // [max_position][D/2] (cos, sin)
+    int32_t* status;
+    int32_t num_pages;
+    int32_t max_position;
+    int32_t hq, hkv, d;
+};
+
+// Record the first device-side error; later ones are dropped.
+__device__ __forceinline__ void record_error(int32_t* status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+// An entry is usable iff its page and every position it covers are in range.
+// Entries failing the check are skipped and reported.
+__device__ __forceinline__ bool entry_ok(const PoolView& pv, uint64_t e) {
+    const int32_t n = entry_nvalid(e);
+    if (n == 0) return true;
+    if (entry_page(e) >= (uint32_t)pv.num_pages || n > kPage ||
+        entry_start(e) + n > pv.max_position) {
+        record_error(pv.status, LAZYATTN_ERANGE);
+        return false;
+    }
+    return true;
+}
+
+// Decode workspace layout (byte offsets from the workspace base).
+struct DecodeWs {
+    size_t qpos_off;      // int32 [R]: logical position of the appended token
+    size_t ticket_off;    // int32 [R*Hkv]: split-combine tickets (zero at rest)
+    size_t ml_off;        // float2 [R*Hkv*S][g]: (m, l) of each split, log2 domain
+    size_t acc_off;       // float [R*Hkv*S][g][D]: unnormalised partial outputs
+    size_t total;
+    int splits;
+};
+
+}  // namespace lazyattn
+
+struct lazyattn_pool {
+    lazyattn_pool_desc d;
+    std::vector<int32_t> free_stack;   // free page ids, lowest id on top
+    std::vector<uint8_t> is_free;
+    int device = 0;
+    int sm_count = 0;
+    int decode_slots = 0;              // resident decode CTAs on the whole GPU
+    lazyattn::PoolView view() const;
+};
+
+namespace lazyattn {
+
+// ---------------------------------------------------------------- launchers
+// Each returns a lazyattn_status; all enqueue on `stream` and never block.
+int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int32_t n_tokens,
+                       const int32_t* pages_host, int32_t npages, cudaStream_t stream);
+int launch_decode_append(const lazyattn_pool& p, const lazyattn_batch& b, const void* k_new,
+                         const void* v_new, int32_t* qpos, cudaStream_t stream);
+int launch_materialize(const lazyattn_pool& p, const lazyattn_batch& b, const uint64_t* dst,
+                       cudaStream_t stream);
+int launch_resolve(const lazyattn_pool& p, const lazyattn_batch& b, const int32_t* out_offsets,
+                   int32_t* out, int32_t cap, cudaStream_t stream);
+
+// fp32 SIMT attention (prefill rows or one decode row per request).
+int launch_attention_f32(const lazyattn_pool& p, const lazyattn_batch& b, const float* q, float* out,
+                         const int32_t* decode_qpos, cudaStream_t stream);
+
+// bf16 decode: split-K over pages, tensor-core dot products (mma.sync), RoPE in registers.
+DecodeWs decode_ws_layout(const lazyattn_pool& p, const lazyattn_batch& b);
+int decode_occupancy(int* ctas_per_sm);
+int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
+                       __nv_bfloat16* out, void* ws, const DecodeWs& L, cudaStream_t stream);
+
+// bf16 prefill on tcgen05 / TMEM with TMA-staged K/V tiles.
+int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
+                        __nv_bfloat16* out, cudaStream_t stream);
+
+}  // namespace lazyattn

@@ -1,0 +1,255 @@
+// Page-level kernels: storing pre-RoPE K/V into pages, the decode-step append,
+// the materialising baseline's copy-and-rotate, and the debug table resolver.
+#include "internal.h"
+
+namespace lazyattn {
+
+namespace {
+
+constexpr int kMaxPagesPerLaunch = 512;
+
+struct PageList {
+    int32_t ids[kMaxPagesPerLaunch];
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// src [n_tokens][Hkv][D] -> pages [page][Hkv][16][D]; one block per (page, kv head).
+// Slots past n_tokens in the last page are zero-filled.
+__global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* kp, uint4* vp,
+                                   int32_t n_tokens, int32_t first_page_index, PageList pages, int hkv,
+                                   int row_vecs) {
+    const int j = blockIdx.x;          // page index within this launch
+    const int h = blockIdx.y;
+    const int32_t page = pages.ids[j];
+    const int tok0 = (first_page_index + j) * kPage;
+    const size_t dst_base = ((size_t)page * hkv + h) * kPage * row_vecs;
+    for (int i = threadIdx.x; i < kPage * row_vecs; i += blockDim.x) {
+        const int slot = i / row_vecs, c = i % row_vecs;
+        const int tok = tok0 + slot;
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (tok < n_tokens) {
+            const size_t src = ((size_t)tok * hkv + h) * row_vecs + c;
+            a = k[src];
+            b = v[src];
+        }
+        kp[dst_base + i] = a;
+        vp[dst_base + i] = b;
+    }
+}
+
+// Find the append slot of request r: first entry with nvalid < 16 in the
+// trailing run of writable entries. Returns the entry index or -1.
+__device__ int find_append_entry(const uint64_t* entries, int e0, int e1) {
+    int tail = -1;
+    for (int i = e1 - 1; i >= e0; --i) {
+        const uint64_t e = entries[i];
+        if (!entry_writable(e)) break;
+        if (entry_nvalid(e) < kPage) tail = i;
+    }
+    return tail;
+}
+
+// One block per request: append k_new/v_new into the request's tail page.
+template <typename T, bool PREROT>
+__global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32_t* entry_offsets,
+                                     const T* __restrict__ k_new, const T* __restrict__ v_new, int32_t* qpos) {
+    const int r = blockIdx.x;
+    __shared__ int s_entry;
+    __shared__ uint64_t s_e;
+    if (threadIdx.x == 0) {
+        const int e0 = entry_offsets[r], e1 = entry_offsets[r + 1];
+        int t = find_append_entry(entries, e0, e1);
+        if (t >= 0) {
+            const uint64_t e = entries[t];
+            const int32_t pos = entry_start(e) + entry_nvalid(e);
+            if (entry_page(e) >= (uint32_t)pv.num_pages || pos >= pv.max_position) {
+                record_error(pv.status, LAZYATTN_ERANGE);
+                t = -1;
+            }
+        } else {
+            record_error(pv.status, LAZYATTN_ENODECODE);
+        }
+        s_entry = t;
+        s_e = t >= 0 ? entries[t] : 0;
+        qpos[r] = t >= 0 ? entry_start(s_e) + entry_nvalid(s_e) : -1;
+    }
+    __syncthreads();
+    if (s_entry < 0) return;
+    const uint64_t e = s_e;
+    const uint32_t page = entry_page(e);
+    const int slot = entry_nvalid(e);
+    const int pos = entry_start(e) + slot;
+    const int D = pv.d, half = D / 2;
+    T* kp = static_cast<T*>(pv.k_pool);
+    T* vp = static_cast<T*>(pv.v_pool);
+    for (int i = threadIdx.x; i < pv.hkv * half; i += blockDim.x) {
+        const int h = i / half, d = i % half;
+        const size_t src = ((size_t)r * pv.hkv + h) * D;
+        const size_t dst = (((size_t)page * pv.hkv + h) * kPage + slot) * D;
+        float k1 = to_f(k_new[src + d]), k2 = to_f(k_new[src + d + half]);
+        if (PREROT) {
+            const float2 cs = pv.rope[(size_t)pos * half + d];
+            const float a = k1 * cs.x - k2 * cs.y;
+            const float b = k1 * cs.y + k2 * cs.x;
+            k1 = a;
+            k2 = b;
+        }
+        kp[dst + d] = from_f<T>(k1);
+        kp[dst + d + half] = from_f<T>(k2);
+        vp[dst + d] = v_new[src + d];
+        vp[dst + d + half] = v_new[src + d + half];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        entries[s_entry] = make_entry(page, entry_start(e), slot + 1, true);
+    }
+}
+
+// One block per (entry slot i of request r): copy the page into dst's page,
+// rotating K at the entry's logical positions.
+template <typename T>
+__global__ void materialize_kernel(PoolView pv, const uint64_t* entries, const int32_t* entry_offsets,
+                                   const uint64_t* dst_entries) {
+    const int r = blockIdx.y;
+    const int idx = entry_offsets[r] + blockIdx.x;
+    if (idx >= entry_offsets[r + 1]) return;
+    const uint64_t e = entries[idx];
+    const uint64_t de = dst_entries[idx];
+    const int n = entry_nvalid(e);
+    if (n == 0) return;
+    if (!entry_ok(pv, e)) return;
+    if (entry_page(de) >= (uint32_t)pv.num_pages) {
+        record_error(pv.status, LAZYATTN_ERANGE);
+        return;
+    }
+    const uint32_t sp = entry_page(e), dp = entry_page(de);
+    const int start = entry_start(e);
+    const int D = pv.d, half = D / 2;
+    const T* ks = static_cast<const T*>(pv.k_pool);
+    const T* vs = static_cast<const T*>(pv.v_pool);
+    T* kd = static_cast<T*>(pv.k_pool);
+    T* vd = static_cast<T*>(pv.v_pool);
+    const int per_head = kPage * half;
+    for (int i = threadIdx.x; i < pv.hkv * per_head; i += blockDim.x) {
+        const int h = i / per_head;
+        const int slot = (i % per_head) / half;
+        const int d = i % half;
+        const size_t so = (((size_t)sp * pv.hkv + h) * kPage + slot) * D;
+        const size_t dso = (((size_t)dp * pv.hkv + h) * kPage + slot) * D;
+        if (slot < n) {
+            const float2 cs = pv.rope[(size_t)(start + slot) * half + d];
+            const float k1 = to_f(ks[so + d]), k2 = to_f(ks[so + d + half]);
+            kd[dso + d] = from_f<T>(k1 * cs.x - k2 * cs.y);
+            kd[dso + d + half] = from_f<T>(k1 * cs.y + k2 * cs.x);
+            vd[dso + d] = vs[so + d];
+            vd[dso + d + half] = vs[so + d + half];
+        } else {
+            kd[dso + d] = from_f<T>(0.f);
+            kd[dso + d + half] = from_f<T>(0.f);
+            vd[dso + d] = from_f<T>(0.f);
+            vd[dso + d + half] = from_f<T>(0.f);
+        }
+    }
+}
+
+// One warp per request: (page, slot, position) of every valid token.
+__global__ void resolve_kernel(const uint64_t* entries, const int32_t* entry_offsets, const int32_t* out_off,
+                               int32_t* out, int32_t cap, int32_t* status) {
+    const int r = blockIdx.x;
+    const int lane = threadIdx.x;
+    const int e0 = entry_offsets[r], e1 = entry_offsets[r + 1];
+    int base = out_off[r];
+    for (int c = e0; c < e1; c += 32) {
+        const int i = c + lane;
+        const uint64_t e = i < e1 ? entries[i] : 0;
+        const int n = i < e1 ? entry_nvalid(e) : 0;
+        int incl = n;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int excl = incl - n;
+        for (int s = 0; s < n; ++s) {
+            const int row = base + excl + s;
+            if (row >= cap) {
+                record_error(status, LAZYATTN_ERANGE);
+                break;
+            }
+            out[3 * row + 0] = (int32_t)entry_page(e);
+            out[3 * row + 1] = s;
+            out[3 * row + 2] = entry_start(e) + s;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+inline int cuda_status() { return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA; }
+
+}  // namespace
+
+int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int32_t n_tokens,
+                       const int32_t* pages_host, int32_t npages, cudaStream_t stream) {
+    const int esz = p.d.dtype == LAZYATTN_F32 ? 4 : 2;
+    const int row_vecs = p.d.head_dim * esz / 16;
+    for (int32_t first = 0; first < npages; first += kMaxPagesPerLaunch) {
+        const int cnt = std::min<int32_t>(kMaxPagesPerLaunch, npages - first);
+        PageList pl;
+        for (int i = 0; i < cnt; ++i) pl.ids[i] = pages_host[first + i];
+        dim3 grid(cnt, p.d.n_kv_heads);
+        store_pages_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                                     static_cast<uint4*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
+                                                     n_tokens, first, pl, p.d.n_kv_heads, row_vecs);
+        if (cuda_status() != LAZYATTN_OK) return LAZYATTN_ECUDA;
+    }
+    return LAZYATTN_OK;
+}
+
+int launch_decode_append(const lazyattn_pool& p, const lazyattn_batch& b, const void* k_new, const void* v_new,
+                         int32_t* qpos, cudaStream_t stream) {
+    const bool pre = (b.flags & LAZYATTN_KEYS_PREROTATED) != 0;
+    const PoolView pv = p.view();
+    if (p.d.dtype == LAZYATTN_F32) {
+        auto kern = pre ? decode_append_kernel<float, true> : decode_append_kernel<float, false>;
+        kern<<<b.num_requests, 128, 0, stream>>>(pv, b.entries, b.entry_offsets, static_cast<const float*>(k_new),
+                                                 static_cast<const float*>(v_new), qpos);
+    } else {
+        auto kern = pre ? decode_append_kernel<__nv_bfloat16, true> : decode_append_kernel<__nv_bfloat16, false>;
+        kern<<<b.num_requests, 128, 0, stream>>>(pv, b.entries, b.entry_offsets,
+                                                 static_cast<const __nv_bfloat16*>(k_new),
+                                                 static_cast<const __nv_bfloat16*>(v_new), qpos);
+    }
+    return cuda_status();
+}
+
+int launch_materialize(const lazyattn_pool& p, const lazyattn_batch& b, const uint64_t* dst, cudaStream_t stream) {
+    const PoolView pv = p.view();
+    dim3 grid(b.max_entries, b.num_requests);
+    if (p.d.dtype == LAZYATTN_F32)
+        materialize_kernel<float><<<grid, 256, 0, stream>>>(pv, b.entries, b.entry_offsets, dst);
+    else
+        materialize_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(pv, b.entries, b.entry_offsets, dst);
+    return cuda_status();
+}
+
+int launch_resolve(const lazyattn_pool& p, const lazyattn_batch& b, const int32_t* out_offsets, int32_t* out,
+                   int32_t cap, cudaStream_t stream) {
+    resolve_kernel<<<b.num_requests, 32, 0, stream>>>(b.entries, b.entry_offsets, out_offsets, out, cap,
+                                                      p.d.status_word);
+    return cuda_status();
+}
+
+}  // namespace lazyattn

@@ -1,0 +1,268 @@
+// Host side of the C ABI: argument validation, the pool's page allocator,
+// position-table construction and kernel dispatch. See include/lazyattn.h.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace lazyattn;
+
+lazyattn::PoolView lazyattn_pool::view() const {
+    PoolView v;
+    v.k_pool = d.k_pool;
+    v.v_pool = d.v_pool;
+    v.rope = static_cast<const float2*>(d.rope_table);
+    v.status = d.status_word;
+    v.num_pages = d.num_pages;
+    v.max_position = d.max_position;
+    v.hq = d.n_q_heads;
+    v.hkv = d.n_kv_heads;
+    v.d = d.head_dim;
+    return v;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+const char* lazyattn_status_string(int s) {
+    switch (s) {
+        case LAZYATTN_OK: return "ok";
+        case LAZYATTN_EINVAL: return "invalid argument";
+        case LAZYATTN_ENOSPC: return "not enough free pages";
+        case LAZYATTN_ERANGE: return "page id or logical position out of range";
+        case LAZYATTN_EDTYPE: return "unsupported dtype for this entry point";
+        case LAZYATTN_ECUDA: return "CUDA runtime error";
+        case LAZYATTN_EDEVICE: return "device-side check failed";
+        case LAZYATTN_EWORKSPACE: return "workspace too small";
+        case LAZYATTN_ENODECODE: return "request has no writable free slot for decode";
+        default: return "unknown status";
+    }
+}
+
+uint64_t lazyattn_pack_entry(int32_t page, int32_t start, int32_t nvalid, int32_t writable) {
+    return make_entry((uint32_t)page, start, nvalid, writable != 0);
+}
+
+size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position) {
+    if (head_dim <= 0 || max_position <= 0) return 0;
+    return (size_t)max_position * (size_t)(head_dim / 2) * sizeof(float2);
+}
+
+int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_pool_t* out_pool) {
+    if (!desc || !out_pool) return LAZYATTN_EINVAL;
+    *out_pool = nullptr;
+    const lazyattn_pool_desc& d = *desc;
+    if (d.num_pages < 1 || d.page_size != kPage || d.n_q_heads < 1 || d.n_kv_heads < 1 ||
+        d.n_q_heads % d.n_kv_heads != 0 || !(d.rope_theta > 0.0) || d.max_position < 1 ||
+        d.max_position > LAZYATTN_MAX_START + kPage)
+        return LAZYATTN_EINVAL;
+    if (!d.k_pool || !d.v_pool || !d.rope_table || !d.status_word) return LAZYATTN_EINVAL;
+    if (!aligned16(d.k_pool) || !aligned16(d.v_pool) || !aligned16(d.rope_table) ||
+        (reinterpret_cast<uintptr_t>(d.status_word) & 3u))
+        return LAZYATTN_EINVAL;
+    if (d.dtype == LAZYATTN_F32) {
+        if (d.head_dim != 64 && d.head_dim != 128) return LAZYATTN_EINVAL;
+    } else if (d.dtype == LAZYATTN_BF16) {
+        if (d.head_dim != 128) return LAZYATTN_EINVAL;
+        if (d.n_q_heads / d.n_kv_heads > 8) return LAZYATTN_EINVAL;   // decode packs <= 8 heads per MMA
+    } else {
+        return LAZYATTN_EDTYPE;
+    }
+
+    lazyattn_pool* p = new (std::nothrow) lazyattn_pool();
+    if (!p) return LAZYATTN_EINVAL;
+    p->d = d;
+    p->is_free.assign((size_t)d.num_pages, 1);
+    p->free_stack.resize((size_t)d.num_pages);
+    for (int32_t i = 0; i < d.num_pages; ++i) p->free_stack[(size_t)i] = d.num_pages - 1 - i;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+        delete p;
+        return LAZYATTN_ECUDA;
+    }
+    int occ = 1;
+    if (d.dtype == LAZYATTN_BF16 && decode_occupancy(&occ) != LAZYATTN_OK) {
+        delete p;
+        return LAZYATTN_ECUDA;
+    }
+    p->decode_slots = p->sm_count * std::max(occ, 1);
+
+    // Position table: angle pos * theta^(-2i/D) in fp64, cos/sin in fp64, stored fp32.
+    const int half = d.head_dim / 2;
+    std::vector<float2> tab((size_t)d.max_position * (size_t)half);
+    std::vector<double> inv(half);
+    for (int i = 0; i < half; ++i) inv[i] = pow(d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
+    for (int32_t pos = 0; pos < d.max_position; ++pos) {
+        float2* row = &tab[(size_t)pos * half];
+        for (int i = 0; i < half; ++i) {
+            const double a = (double)pos * inv[i];
+            row[i] = make_float2((float)cos(a), (float)sin(a));
+        }
+    }
+    cudaError_t e = cudaMemcpyAsync(d.rope_table, tab.data(), tab.size() * sizeof(float2),
+                                    cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d.status_word, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        delete p;
+        return LAZYATTN_ECUDA;
+    }
+    *out_pool = p;
+    return LAZYATTN_OK;
+}
+
+int lazyattn_pool_destroy(lazyattn_pool_t pool) {
+    if (!pool) return LAZYATTN_EINVAL;
+    delete pool;
+    return LAZYATTN_OK;
+}
+
+int lazyattn_pool_free_count(lazyattn_pool_t pool, int32_t* out_count) {
+    if (!pool || !out_count) return LAZYATTN_EINVAL;
+    *out_count = (int32_t)pool->free_stack.size();
+    return LAZYATTN_OK;
+}
+
+int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages) {
+    if (!pool || n < 0 || (n > 0 && !out_pages)) return LAZYATTN_EINVAL;
+    if ((size_t)n > pool->free_stack.size()) return LAZYATTN_ENOSPC;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t pg = pool->free_stack.back();
+        pool->free_stack.pop_back();
+        pool->is_free[(size_t)pg] = 0;
+        out_pages[i] = pg;
+    }
+    return LAZYATTN_OK;
+}
+
+int lazyattn_free_pages(lazyattn_pool_t pool, const int32_t* pages, int32_t n) {
+    if (!pool || n < 0 || (n > 0 && !pages)) return LAZYATTN_EINVAL;
+    std::vector<int32_t> seen;
+    seen.reserve((size_t)n);
+    for (int32_t i = 0; i < n; ++i) {
+        if (pages[i] < 0 || pages[i] >= pool->d.num_pages) return LAZYATTN_ERANGE;
+        if (pool->is_free[(size_t)pages[i]]) return LAZYATTN_EINVAL;
+        seen.push_back(pages[i]);
+    }
+    std::sort(seen.begin(), seen.end());
+    if (std::adjacent_find(seen.begin(), seen.end()) != seen.end()) return LAZYATTN_EINVAL;
+    // Keep the stack ordered so that the lowest free id is handed out first.
+    for (int32_t pg : seen) pool->is_free[(size_t)pg] = 1;
+    pool->free_stack.insert(pool->free_stack.end(), seen.begin(), seen.end());
+    std::sort(pool->free_stack.begin(), pool->free_stack.end(), std::greater<int32_t>());
+    return LAZYATTN_OK;
+}
+
+int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32_t n_tokens, void* stream,
+                       int32_t* out_pages, int32_t out_cap, int32_t* out_npages) {
+    if (!pool || !k || !v || !out_pages || !out_npages || n_tokens < 1) return LAZYATTN_EINVAL;
+    if (!aligned16(k) || !aligned16(v)) return LAZYATTN_EINVAL;
+    const int32_t np = (n_tokens + kPage - 1) / kPage;
+    if (out_cap < np) return LAZYATTN_EINVAL;
+    int rc = lazyattn_alloc_pages(pool, np, out_pages);
+    if (rc != LAZYATTN_OK) return rc;
+    rc = launch_store_pages(*pool, k, v, n_tokens, out_pages, np, static_cast<cudaStream_t>(stream));
+    if (rc != LAZYATTN_OK) {
+        lazyattn_free_pages(pool, out_pages, np);
+        return rc;
+    }
+    *out_npages = np;
+    return LAZYATTN_OK;
+}
+
+static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int op) {
+    if (!pool || !b) return LAZYATTN_EINVAL;
+    if (b->num_requests < 1 || b->max_entries < 0 || !b->entries || !b->entry_offsets) return LAZYATTN_EINVAL;
+    if (b->flags & ~LAZYATTN_KEYS_PREROTATED) return LAZYATTN_EINVAL;
+    if (op == LAZYATTN_OP_PREFILL) {
+        if (b->total_q < 0 || b->max_q_len < 0 || !b->q_offsets || !b->q_start) return LAZYATTN_EINVAL;
+    }
+    return LAZYATTN_OK;
+}
+
+size_t lazyattn_workspace_size(lazyattn_pool_t pool, int32_t op, const lazyattn_batch* batch) {
+    if (check_batch(pool, batch, op) != LAZYATTN_OK) return 0;
+    if (op == LAZYATTN_OP_PREFILL) return 256;
+    if (op != LAZYATTN_OP_DECODE) return 0;
+    if (pool->d.dtype == LAZYATTN_F32) return (size_t)batch->num_requests * sizeof(int32_t) + 256;
+    return decode_ws_layout(*pool, *batch).total;
+}
+
+int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q, void* out,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_batch(pool, batch, LAZYATTN_OP_PREFILL);
+    if (rc != LAZYATTN_OK) return rc;
+    if (batch->total_q == 0) return LAZYATTN_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return LAZYATTN_EINVAL;
+    (void)workspace;
+    (void)workspace_bytes;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (pool->d.dtype == LAZYATTN_F32)
+        return launch_attention_f32(*pool, *batch, static_cast<const float*>(q), static_cast<float*>(out),
+                                    nullptr, st);
+    return launch_prefill_bf16(*pool, *batch, static_cast<const __nv_bfloat16*>(q),
+                               static_cast<__nv_bfloat16*>(out), st);
+}
+
+int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q, const void* k_new,
+                    const void* v_new, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
+    if (rc != LAZYATTN_OK) return rc;
+    if (!q || !k_new || !v_new || !out || !workspace) return LAZYATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return LAZYATTN_EINVAL;
+    if (workspace_bytes < lazyattn_workspace_size(pool, LAZYATTN_OP_DECODE, batch)) return LAZYATTN_EWORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (pool->d.dtype == LAZYATTN_F32) {
+        int32_t* qpos = static_cast<int32_t*>(workspace);
+        rc = launch_decode_append(*pool, *batch, k_new, v_new, qpos, st);
+        if (rc != LAZYATTN_OK) return rc;
+        return launch_attention_f32(*pool, *batch, static_cast<const float*>(q), static_cast<float*>(out),
+                                    qpos, st);
+    }
+    const DecodeWs L = decode_ws_layout(*pool, *batch);
+    int32_t* qpos = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.qpos_off);
+    rc = launch_decode_append(*pool, *batch, k_new, v_new, qpos, st);
+    if (rc != LAZYATTN_OK) return rc;
+    return launch_decode_bf16(*pool, *batch, static_cast<const __nv_bfloat16*>(q),
+                              static_cast<__nv_bfloat16*>(out), workspace, L, st);
+}
+
+int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch, const uint64_t* dst_entries,
+                         void* stream) {
+    int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
+    if (rc != LAZYATTN_OK) return rc;
+    if (!dst_entries || (batch->flags & LAZYATTN_KEYS_PREROTATED)) return LAZYATTN_EINVAL;
+    if (batch->max_entries == 0) return LAZYATTN_OK;
+    return launch_materialize(*pool, *batch, dst_entries, static_cast<cudaStream_t>(stream));
+}
+
+int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const int32_t* out_offsets,
+                     int32_t* out_triples, int32_t out_cap, void* stream) {
+    int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
+    if (rc != LAZYATTN_OK) return rc;
+    if (!out_offsets || !out_triples || out_cap < 0) return LAZYATTN_EINVAL;
+    return launch_resolve(*pool, *batch, out_offsets, out_triples, out_cap, static_cast<cudaStream_t>(stream));
+}
+
+int lazyattn_get_device_status(lazyattn_pool_t pool, int32_t* out_status, int32_t reset, void* stream) {
+    if (!pool || !out_status) return LAZYATTN_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, pool->d.status_word, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && reset) e = cudaMemsetAsync(pool->d.status_word, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return LAZYATTN_ECUDA;
+    *out_status = h;
+    return LAZYATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+"""Host-side plumbing around the C ABI: device buffers (torch) and block tables.
+
+DevicePool allocates the caller-owned buffers a lazyattn pool needs (K/V pools,
+position table, status word) with torch and creates the pool through the C ABI.
+build_batch packs per-request page lists into the 64-bit entry format of
+lazyattn_pack_entry and uploads the table. No attention arithmetic happens here.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Sequence
+
+import numpy as np
+import torch
+
+from . import lazyattn as L
+
+PAGE_SIZE = L.PAGE_SIZE
+
+
+def pack_entries(pages, starts, nvalid, writable) -> np.ndarray:
+    """Vectorised lazyattn_pack_entry (same bit layout) for whole tables."""
+    pages = np.asarray(pages, np.uint64) & np.uint64(0xFFFFFFFF)
+    starts = (np.asarray(starts, np.uint64) & np.uint64((1 << 26) - 1)) << np.uint64(32)
+    nvalid = (np.asarray(nvalid, np.uint64) & np.uint64(0x1F)) << np.uint64(58)
+    writable = (np.asarray(writable, np.uint64) & np.uint64(1)) << np.uint64(63)
+    return pages | starts | nvalid | writable
+
+
+@dataclasses.dataclass
+class Segment:
+    """A run of tokens stored in consecutive entries: page ids, logical start,
+    token count, and whether decode may append into its pages."""
+    pages: Sequence[int]
+    start: int
+    n_tokens: int
+    writable: bool = False
+
+
+class DevicePool:
+    def __init__(self, num_pages: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: str,
+                 rope_theta: float, max_position: int, device="cuda", stream=None):
+        self.dtype = dtype
+        self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
+        self.num_pages = num_pages
+        self.max_position = max_position
+        shape = (num_pages, n_kv_heads, PAGE_SIZE, head_dim)
+        self.k_pool = torch.zeros(shape, dtype=self.tdtype, device=device)
+        self.v_pool = torch.zeros(shape, dtype=self.tdtype, device=device)
+        self.rope_table = torch.empty(L.lazyattn_rope_table_bytes(head_dim, max_position) // 4,
+                                      dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.desc = L.lazyattn_pool_desc(num_pages, PAGE_SIZE, n_q_heads, n_kv_heads, head_dim,
+                                         L.LAZYATTN_F32 if dtype == "f32" else L.LAZYATTN_BF16,
+                                         float(rope_theta), max_position, self.k_pool.data_ptr(),
+                                         self.v_pool.data_ptr(), self.rope_table.data_ptr(),
+                                         self.status.data_ptr())
+        self.handle = L.lazyattn_pool_create(self.desc, stream)
+
+    def close(self):
+        if self.handle:
+            L.lazyattn_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def store_doc(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> List[int]:
+        assert k.is_contiguous() and v.is_contiguous() and k.dtype == self.tdtype
+        return L.lazyattn_store_doc(self.handle, k, v, int(k.shape[0]), stream)
+
+    def alloc_pages(self, n: int) -> List[int]:
+        return L.lazyattn_alloc_pages(self.handle, n)
+
+    def free_pages(self, pages: Sequence[int]):
+        L.lazyattn_free_pages(self.handle, list(pages))
+
+    def free_count(self) -> int:
+        return L.lazyattn_pool_free_count(self.handle)
+
+    def device_status(self, reset=True, stream=None) -> int:
+        return L.lazyattn_get_device_status(self.handle, reset, stream)
+
+
+def segment_entries(seg: Segment):
+    n_pages = len(seg.pages)
+    assert n_pages * PAGE_SIZE >= seg.n_tokens
+    nvalid = [max(0, min(PAGE_SIZE, seg.n_tokens - j * PAGE_SIZE)) for j in range(n_pages)]
+    starts = [seg.start + j * PAGE_SIZE for j in range(n_pages)]
+    return list(seg.pages), starts, nvalid, [int(seg.writable)] * n_pages
+
+
+class Batch:
+    """Device-side block table (and prefill query layout) for a set of requests."""
+
+    def __init__(self, requests: Sequence[Sequence[Segment]], q_lens: Sequence[int] = (),
+                 q_starts: Sequence[int] = (), device="cuda", flags: int = 0):
+        pg, st, nv, wr, offs = [], [], [], [], [0]
+        for segs in requests:
+            for seg in segs:
+                a, b, c, d = segment_entries(seg)
+                pg += a; st += b; nv += c; wr += d
+            offs.append(len(pg))
+        self.entries_host = pack_entries(pg, st, nv, wr) if pg else np.zeros(0, np.uint64)
+        self.offsets_host = np.array(offs, np.int32)
+        self.num_requests = len(requests)
+        self.max_entries = int(np.max(np.diff(self.offsets_host))) if len(requests) else 0
+        self.entries = torch.from_numpy(self.entries_host.view(np.int64).copy()).to(device)
+        if self.entries.numel() == 0:
+            self.entries = torch.zeros(1, dtype=torch.int64, device=device)
+        self.entry_offsets = torch.from_numpy(self.offsets_host).to(device)
+        q_lens = list(q_lens)
+        if q_lens:
+            qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+            self.q_offsets = torch.from_numpy(qo).to(device)
+            self.q_start = torch.tensor(list(q_starts), dtype=torch.int32, device=device)
+            self.total_q = int(qo[-1])
+            self.max_q_len = int(max(q_lens))
+        else:
+            self.q_offsets = self.q_start = None
+            self.total_q = self.max_q_len = 0
+        self.flags = flags
+        self.c = L.make_batch(self.num_requests, self.max_entries, self.entries, self.entry_offsets,
+                              self.q_offsets, self.q_start, self.max_q_len, self.total_q, flags)
+
+    def with_entries(self, entries_host: np.ndarray, flags: int, device="cuda") -> "Batch":
+        """Same requests and query layout, another entry array (e.g. materialised pages)."""
+        b = Batch.__new__(Batch)
+        b.__dict__.update(self.__dict__)
+        b.entries_host = entries_host.astype(np.uint64)
+        b.entries = torch.from_numpy(b.entries_host.view(np.int64).copy()).to(device)
+        b.flags = flags
+        b.c = L.make_batch(b.num_requests, b.max_entries, b.entries, b.entry_offsets, b.q_offsets, b.q_start,
+                           b.max_q_len, b.total_q, flags)
+        return b

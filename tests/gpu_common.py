@@ -1,0 +1,60 @@
+"""Shared helpers of the GPU parity tests: tolerances and oracle references."""
+import functools
+
+import numpy as np
+
+import oracle
+import workload
+
+# Tolerances (GPU vs fp64 oracle on the same, already rounded, inputs)
+F32_MAX_ABS = 1e-4
+BF16_MAX_ABS = 2e-2
+BF16_REL_L2 = 5e-3
+
+
+def compare(got, ref, dtype):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    err = got - ref
+    max_abs = float(np.max(np.abs(err))) if err.size else 0.0
+    rel = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300))
+    if dtype == "f32":
+        assert max_abs <= F32_MAX_ABS, f"max-abs {max_abs:.3e} > {F32_MAX_ABS}"
+    else:
+        assert max_abs <= BF16_MAX_ABS, f"max-abs {max_abs:.3e} > {BF16_MAX_ABS}"
+        assert rel <= BF16_REL_L2, f"rel-L2 {rel:.3e} > {BF16_REL_L2}"
+    return max_abs, rel
+
+
+class Reference:
+    """fp64 oracle outputs for a workload config, computed per request on demand."""
+
+    def __init__(self, cfg):
+        self.cfg = cfg
+        self.docs = workload.request_docs(cfg)
+
+    @functools.lru_cache(maxsize=None)
+    def doc(self, d):
+        return workload.doc_kv(self.cfg, d)
+
+    def ctx(self, r):
+        return [self.doc(int(d)) for d in self.docs[r]]
+
+    def qseg(self, r):
+        cfg = self.cfg
+        if cfg.q_len:
+            return workload.query_segment(cfg, r)
+        H = np.zeros((0, cfg.n_q_heads, cfg.head_dim), np.float32)
+        K = np.zeros((0, cfg.n_kv_heads, cfg.head_dim), np.float32)
+        return H, K, K.copy()
+
+    def prefill(self, r):
+        q, kq, vq = self.qseg(r)
+        return oracle.prefill_request(self.ctx(r), q, kq, vq, self.cfg.rope_theta)
+
+    def decode(self, r, n_steps):
+        _, kq, vq = self.qseg(r)
+        steps = [tuple(a[0] for a in workload.decode_inputs(self.cfg, t, [r])) for t in range(n_steps)]
+        return oracle.decode_request(self.ctx(r), kq, vq, steps, self.cfg.rope_theta)

@@ -1,0 +1,70 @@
+"""Upload a synthetic workload into a lazyattn pool on the GPU.
+
+Stores every pool document (pre-RoPE K/V) with lazyattn_store_doc, stores each
+request's query-segment K/V in private writable pages, reserves writable pages
+for generated tokens, and builds the block tables. Input plumbing only.
+"""
+from __future__ import annotations
+
+import types
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import Config, PAGE_SIZE, decode_inputs, doc_kv, query_segment, request_docs
+
+
+def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+    return t if dtype == "f32" else t.to(torch.bfloat16)
+
+
+def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool = False,
+          extra_pages: int = 0, device="cuda", all_docs: bool = True):
+    """Build pool + tables for `requests` (default: all) of cfg.
+
+    all_docs=False stores only the documents those requests use (the pool is
+    still sized for every document). baseline=True reserves room for the
+    materialising baseline's private copies.
+    """
+    from position_agnostic_kv_lazyattn_gb300 import Batch, DevicePool, Segment
+
+    reqs = list(range(cfg.n_requests)) if requests is None else list(requests)
+    docs = request_docs(cfg)
+    R = len(reqs)
+    per_req = cfg.q_pages + cfg.decode_pages
+    base_pages = R * cfg.docs_per_request * cfg.doc_pages if baseline else 0
+    num_pages = cfg.n_docs * cfg.doc_pages + R * per_req + base_pages + extra_pages
+    pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
+                      cfg.max_position, device)
+    doc_ids = range(cfg.n_docs) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
+    doc_pages = {}
+    for d in doc_ids:
+        k, v = doc_kv(cfg, d)
+        doc_pages[d] = pool.store_doc(to_device(k, cfg.dtype, device), to_device(v, cfg.dtype, device))
+    segs, qs = [], []
+    for r in reqs:
+        s = []
+        for i, d in enumerate(docs[r]):
+            s.append(Segment(doc_pages[int(d)], i * cfg.doc_len, cfg.doc_len, False))
+        if cfg.q_len:
+            q, kq, vq = query_segment(cfg, r)
+            qs.append(q)
+            pages = pool.store_doc(to_device(kq, cfg.dtype, device), to_device(vq, cfg.dtype, device))
+            s.append(Segment(pages, cfg.context_len, cfg.q_len, True))
+        if cfg.decode_pages:
+            pages = pool.alloc_pages(cfg.decode_pages)
+            s.append(Segment(pages, cfg.context_len + cfg.q_pages * PAGE_SIZE, 0, True))
+        segs.append(s)
+    q_lens = [cfg.q_len] * R if cfg.q_len else []
+    batch = Batch(segs, q_lens, [cfg.context_len] * R if cfg.q_len else [], device)
+    q = to_device(np.concatenate(qs), cfg.dtype, device) if qs else None
+    torch.cuda.synchronize()
+    return types.SimpleNamespace(cfg=cfg, pool=pool, batch=batch, q=q, requests=reqs, docs=docs,
+                                 doc_pages=doc_pages, segments=segs)
+
+
+def decode_step_tensors(cfg: Config, step: int, requests: Sequence[int], device="cuda"):
+    q, k, v = decode_inputs(cfg, step, requests)
+    return to_device(q, cfg.dtype, device), to_device(k, cfg.dtype, device), to_device(v, cfg.dtype, device)
