@@ -202,20 +202,22 @@ def run_ours(args, rank, world):
         return None
 
     # baseline (same box, same inputs)
-    for _ in range(max(1, args.warmup // 2)):
-        base_step([])
-    torch.cuda.synchronize()
-    brec = []
-    for _ in range(max(1, min(args.steps, 3))):
-        base_step(brec)
-    torch.cuda.synchronize()
-    b_mat = statistics.mean(r[0].elapsed_time(r[1]) for r in brec)
-    b_pre = statistics.mean(r[1].elapsed_time(r[2]) for r in brec)
-    b_dec = statistics.mean(r[2].elapsed_time(r[3]) for r in brec)
+    b_mat = b_pre = b_dec = None
+    if not args.no_extras:
+        for _ in range(max(1, args.warmup // 2)):
+            base_step([])
+        torch.cuda.synchronize()
+        brec = []
+        for _ in range(max(1, min(args.steps, 3))):
+            base_step(brec)
+        torch.cuda.synchronize()
+        b_mat = statistics.mean(r[0].elapsed_time(r[1]) for r in brec)
+        b_pre = statistics.mean(r[1].elapsed_time(r[2]) for r in brec)
+        b_dec = statistics.mean(r[2].elapsed_time(r[3]) for r in brec)
 
     # end to end through host buffers (pinned), copies inside the timed region
     e2e = None
-    if cfg.decode_steps:
+    if cfg.decode_steps and not args.no_extras:
         host_in = [tuple(x.cpu().pin_memory() for x in dec_in[t]) for t in range(cfg.decode_steps)]
         host_out = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
         dq = torch.empty_like(dec_in[0][0]); dk = torch.empty_like(dec_in[0][1]); dv = torch.empty_like(dec_in[0][2])
@@ -264,11 +266,12 @@ def run_ours(args, rank, world):
         "prefill_roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(pre_tflops, 2),
                              "peak": tc_peak, "unit": "TFLOP/s", "frac": round(pre_tflops / tc_peak, 4),
                              "peak_kind": peak_kind},
-        "materialising_baseline": {"materialise_ms": round(b_mat, 4), "ttft_ms": round(b_mat + b_pre, 4),
-                                   "decode_ms": round(b_dec, 4),
-                                   "decode_gbs": round(dec_total_bytes / (b_dec / 1e3) / 1e9, 1) if b_dec else None,
-                                   "lazy_ttft_speedup": round((b_mat + b_pre) / local["pre_ms"], 3),
-                                   "lazy_step_speedup": round((b_mat + b_pre + b_dec) / local["step_ms"], 3)},
+        "materialising_baseline": None if b_mat is None else {
+            "materialise_ms": round(b_mat, 4), "ttft_ms": round(b_mat + b_pre, 4), "decode_ms": round(b_dec, 4),
+            "decode_gbs": round(dec_total_bytes / (b_dec / 1e3) / 1e9, 1) if b_dec else None,
+            "lazy_ttft_speedup": round((b_mat + b_pre) / local["pre_ms"], 3) if local["pre_ms"] else None,
+            "lazy_decode_speedup": round(b_dec / (local["dec_s"] * 1e3), 3) if local["dec_s"] else None,
+            "lazy_step_speedup": round((b_mat + b_pre + b_dec) / local["step_ms"], 3)},
         "e2e": e2e,
         "gpu_launches": args.steps * ((1 if cfg.q_len else 0) + 2 * cfg.decode_steps),
         "wall_s_timed": round(local["wall"], 4),
@@ -355,6 +358,7 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the baseline and end-to-end legs")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

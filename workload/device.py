@@ -34,7 +34,7 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     docs = request_docs(cfg)
     R = len(reqs)
     per_req = cfg.q_pages + cfg.decode_pages
-    base_pages = R * cfg.docs_per_request * cfg.doc_pages if baseline else 0
+    base_pages = R * (cfg.docs_per_request * cfg.doc_pages + per_req) if baseline else 0
     num_pages = cfg.n_docs * cfg.doc_pages + R * per_req + base_pages + extra_pages
     pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
                       cfg.max_position, device)
