@@ -236,6 +236,28 @@ int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const in
  * reset; otherwise a negative lazyattn_status. */
 int lazyattn_get_device_status(lazyattn_pool_t pool, int32_t* out_status, int32_t reset, void* stream);
 
+/* Decode step that allocates nothing (no counterpart in the paper).
+ * For callers that cannot obtain device memory for lazyattn_decode's workspace:
+ * code whose host owns every device allocation, allocator-less runtimes, or
+ * contexts that must not grow after start-up. Same arguments, semantics and
+ * results as lazyattn_decode, without the workspace: scratch comes from a
+ * fixed array of LAZYATTN_NOALLOC_SCRATCH_BYTES inside the library (device
+ * global memory; every GPU that loads the library holds one until the process
+ * exits). The call makes no cudaMalloc/cudaFree and no allocating library call.
+ *   - Returns LAZYATTN_EWORKSPACE, launching nothing, if the batch needs more
+ *     scratch than that (lazyattn_workspace_size(pool, LAZYATTN_OP_DECODE, b)
+ *     tells how much it needs).
+ *   - The pool's device must be current. The first call on a device looks up
+ *     the array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents (the call clears what must start at zero). Calls that overlap
+ *     on the GPU - on different streams, or from different threads - race on
+ *     it: serialise them. */
+#define LAZYATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int lazyattn_decode_noalloc(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q,
+                            const void* k_new, const void* v_new, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

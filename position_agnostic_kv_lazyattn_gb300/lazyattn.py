@@ -75,6 +75,7 @@ def _load():
         "lazyattn_materialize": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp]),
         "lazyattn_resolve": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp, i32, vp]),
         "lazyattn_get_device_status": (ctypes.c_int, [vp, P_i32, i32, vp]),
+        "lazyattn_decode_noalloc": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -88,8 +89,9 @@ EXPORTS = [
     "lazyattn_status_string", "lazyattn_pack_entry", "lazyattn_rope_table_bytes", "lazyattn_pool_create",
     "lazyattn_pool_destroy", "lazyattn_pool_free_count", "lazyattn_alloc_pages", "lazyattn_free_pages",
     "lazyattn_store_doc", "lazyattn_workspace_size", "lazyattn_prefill", "lazyattn_decode",
-    "lazyattn_materialize", "lazyattn_resolve", "lazyattn_get_device_status",
+    "lazyattn_materialize", "lazyattn_resolve", "lazyattn_get_device_status", "lazyattn_decode_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def _check(rc: int, where: str):
@@ -186,6 +188,13 @@ def lazyattn_decode(pool: int, batch: lazyattn_batch, q, k_new, v_new, out, work
                     stream=None):
     _check(lib.lazyattn_decode(pool, ctypes.byref(batch), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                _ptr(workspace), workspace_bytes, _stream(stream)), "lazyattn_decode")
+
+
+def lazyattn_decode_noalloc(pool: int, batch: lazyattn_batch, q, k_new, v_new, out, stream=None):
+    """lazyattn_decode without a workspace, for callers that cannot allocate
+    device memory: uses the library's built-in scratch array instead."""
+    _check(lib.lazyattn_decode_noalloc(pool, ctypes.byref(batch), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                       _stream(stream)), "lazyattn_decode_noalloc")
 
 
 def lazyattn_materialize(pool: int, batch: lazyattn_batch, dst_entries, stream=None):
