@@ -115,7 +115,10 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     cfg = workload.CONFIGS[args.config]
-    env = wdev.setup(cfg, baseline=True)
+    if args.requests:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_requests=min(args.requests, cfg.n_requests))
+    env = wdev.setup(cfg, baseline=not args.no_extras)
     R = cfg.n_requests
     b = env.batch
     stream = torch.cuda.current_stream()
@@ -132,43 +135,62 @@ def run_ours(args, rank, world):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # > 129 MB L2
 
     # materialising baseline: private copies of every entry's page
-    base_pages = env.pool.alloc_pages(len(b.entries_host))
-    dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.array(base_pages, np.uint64)
-    dst_dev = torch.from_numpy(dst.view(np.int64).copy()).to(dev)
-    mb = b.with_entries(dst, L.LAZYATTN_KEYS_PREROTATED, device=dev)
-    mb_entries0 = mb.entries.clone()
+    if not args.no_extras:
+        base_pages = env.pool.alloc_pages(len(b.entries_host))
+        dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.array(base_pages, np.uint64)
+        dst_dev = torch.from_numpy(dst.view(np.int64).copy()).to(dev)
+        mb = b.with_entries(dst, L.LAZYATTN_KEYS_PREROTATED, device=dev)
+        mb_entries0 = mb.entries.clone()
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
+    # One CUDA graph per phase: the prefill launch, and the decode steps (append +
+    # attention each). Replays remove host launch gaps from the timed region.
+    def capture(fn):
+        fn()                                    # eager run first (also a warm-up)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def prefill_lazy():
+        if b.total_q:
+            L.lazyattn_prefill(env.pool.handle, b.c, env.q, out_p, None, 0, None)
+
+    def decode_lazy():
+        for t in range(cfg.decode_steps):
+            q, k, v = dec_in[t]
+            L.lazyattn_decode(env.pool.handle, b.c, q, k, v, out_d, ws, ws_bytes, None)
+
+    def materialize_base():
+        L.lazyattn_materialize(env.pool.handle, b.c, dst_dev, None)
+
+    def prefill_base():
+        if b.total_q:
+            L.lazyattn_prefill(env.pool.handle, mb.c, env.q, out_p, None, 0, None)
+
+    def decode_base():
+        for t in range(cfg.decode_steps):
+            q, k, v = dec_in[t]
+            L.lazyattn_decode(env.pool.handle, mb.c, q, k, v, out_d, ws, ws_bytes, None)
+
+    g_pre = capture(prefill_lazy)
+    b.entries.copy_(entries0)
+    g_dec = capture(decode_lazy)
+    b.entries.copy_(entries0)
+
     def lazy_step(rec):
         b.entries.copy_(entries0)
         flush.zero_()
-        e = [ev() for _ in range(cfg.decode_steps + 2)]
+        e = [ev(), ev(), ev()]
         e[0].record(stream)
-        if b.total_q:
-            L.lazyattn_prefill(env.pool.handle, b.c, env.q, out_p, None, 0, stream)
+        g_pre.replay()
         e[1].record(stream)
-        for t in range(cfg.decode_steps):
-            q, k, v = dec_in[t]
-            L.lazyattn_decode(env.pool.handle, b.c, q, k, v, out_d, ws, ws_bytes, stream)
-            e[t + 2].record(stream)
-        rec.append(e)
-
-    def base_step(rec):
-        mb.entries.copy_(mb_entries0)
-        flush.zero_()
-        e = [ev() for _ in range(4)]
-        e[0].record(stream)
-        L.lazyattn_materialize(env.pool.handle, b.c, dst_dev, stream)
-        e[1].record(stream)
-        if b.total_q:
-            L.lazyattn_prefill(env.pool.handle, mb.c, env.q, out_p, None, 0, stream)
+        g_dec.replay()
         e[2].record(stream)
-        for t in range(cfg.decode_steps):
-            q, k, v = dec_in[t]
-            L.lazyattn_decode(env.pool.handle, mb.c, q, k, v, out_d, ws, ws_bytes, stream)
-        e[3].record(stream)
         rec.append(e)
 
     def barrier():
@@ -190,8 +212,8 @@ def run_ours(args, rank, world):
     status = env.pool.device_status()
 
     pre_ms = [r[0].elapsed_time(r[1]) for r in rec]
-    dec_ms = [r[1].elapsed_time(r[-1]) for r in rec]
-    dec_call_ms = [r[t + 1].elapsed_time(r[t + 2]) for r in rec for t in range(cfg.decode_steps)]
+    dec_ms = [r[1].elapsed_time(r[2]) for r in rec]
+    dec_call_ms = [d / max(cfg.decode_steps, 1) for d in dec_ms]
     step_ms = [p + d for p, d in zip(pre_ms, dec_ms)]
     dec_total_bytes = sum(dec_bytes)
     mean_dec_s = statistics.mean(dec_ms) / 1e3
@@ -201,15 +223,27 @@ def run_ours(args, rank, world):
     if rank != 0:
         return None
 
-    # baseline (same box, same inputs)
+    # baseline (same box, same inputs): materialise, prefill and decode on private rotated copies
     b_mat = b_pre = b_dec = None
     if not args.no_extras:
-        for _ in range(max(1, args.warmup // 2)):
-            base_step([])
-        torch.cuda.synchronize()
+        g_bmat = capture(materialize_base)
+        g_bpre = capture(prefill_base)
+        mb.entries.copy_(mb_entries0)
+        g_bdec = capture(decode_base)
         brec = []
-        for _ in range(max(1, min(args.steps, 3))):
-            base_step(brec)
+        for it in range(max(2, min(args.steps, 20)) + 2):
+            mb.entries.copy_(mb_entries0)
+            flush.zero_()
+            e = [ev() for _ in range(4)]
+            e[0].record(stream)
+            g_bmat.replay()
+            e[1].record(stream)
+            g_bpre.replay()
+            e[2].record(stream)
+            g_bdec.replay()
+            e[3].record(stream)
+            if it >= 2:
+                brec.append(e)
         torch.cuda.synchronize()
         b_mat = statistics.mean(r[0].elapsed_time(r[1]) for r in brec)
         b_pre = statistics.mean(r[1].elapsed_time(r[2]) for r in brec)
@@ -258,6 +292,7 @@ def run_ours(args, rank, world):
                    "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}"},
         "prefill_tflops": round(pre_tflops, 2), "ttft_ms": round(local["pre_ms"], 4),
         "decode_ms_per_token_step": round(mean_call, 4),
+        "timing": "CUDA events around CUDA-graph replays (prefill graph; graph of all decode steps)",
         "frac_hbm_peak": round(dec_gbs / world / hbm_peak, 4),
         "frac_tensor_peak": round(pre_tflops / world / tc_peak, 4),
         "roofline": {"kernel": "lazyattn_decode (append + split-K attention)", "bound": "hbm",
@@ -353,12 +388,13 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the baseline and end-to-end legs")
+    ap.add_argument("--requests", type=int, default=0, help="use only the first N requests (profiling captures)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

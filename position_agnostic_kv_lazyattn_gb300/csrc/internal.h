@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -73,6 +74,8 @@ struct lazyattn_pool {
     int device = 0;
     int sm_count = 0;
     int decode_slots = 0;              // resident decode CTAs on the whole GPU
+    bool have_maps = false;            // bf16 pools: TMA views of the K and V pools
+    CUtensorMap kmap, vmap;
     lazyattn::PoolView view() const;
 };
 
@@ -89,6 +92,11 @@ int launch_materialize(const lazyattn_pool& p, const lazyattn_batch& b, const ui
 int launch_resolve(const lazyattn_pool& p, const lazyattn_batch& b, const int32_t* out_offsets,
                    int32_t* out, int32_t cap, cudaStream_t stream);
 
+// TMA views of the bf16 K and V pools as rows of 128 elements (row = (page *
+// Hkv + kv head) * 16 + slot), 64 x 16 boxes, 128-byte swizzle. False if the
+// driver entry point is unavailable or the pool is too large for 32-bit rows.
+bool encode_pool_maps(lazyattn_pool& p);
+
 // fp32 SIMT attention (prefill rows or one decode row per request).
 int launch_attention_f32(const lazyattn_pool& p, const lazyattn_batch& b, const float* q, float* out,
                          const int32_t* decode_qpos, cudaStream_t stream);
@@ -99,7 +107,10 @@ int decode_occupancy(int* ctas_per_sm);
 int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
                        __nv_bfloat16* out, void* ws, const DecodeWs& L, cudaStream_t stream);
 
-// bf16 prefill on tcgen05 / TMEM with TMA-staged K/V tiles.
+// bf16 prefill on tcgen05 / TMEM with TMA-staged K/V tiles. prefill_init()
+// sets the kernel's shared-memory limit on the current device (done once, at
+// pool creation, so that launches stay capturable in CUDA graphs).
+int prefill_init();
 int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
                         __nv_bfloat16* out, cudaStream_t stream);
 

@@ -1,37 +1,48 @@
 // bf16 decode attention: one query token per request over its paged,
 // position-free KV, with RoPE applied to every key in registers at its logical
 // position (LazyAttention §3.2 "Decoding"; §3.4: decode stays at ~2LD bytes of
-// HBM traffic, the rotation happens on chip).
+// HBM traffic because the rotation happens on chip).
 //
 // Work split: a CTA owns (request r, KV head h, split s) and a contiguous run of
-// the request's pages; its four warps take pages round-robin. Per page (16
-// tokens x 128 dims, one contiguous 4 KB tile each for K and V) a warp:
-//   * loads K rows and V rows with 16-byte loads straight into registers,
-//   * rotates K at positions start..start+15 (cos/sin from the fp32 position
-//     table), converting to fp16 (10-bit mantissa keeps the rotated key close to
-//     its fp32 value),
-//   * computes S^T = K' Q'^T with m16n8k16 MMAs: 16 tokens x up to 8 query
-//     heads of the group, 128-deep,
-//   * does the online softmax in the log2 domain (q is pre-scaled by
+// the request's pages; its four warps take the run's pages round-robin. Each
+// warp keeps its own ring of three page stages in shared memory, filled by TMA
+// (lane 0 issues; K and V tiles of one page are 4 KB each, two 64-dim boxes with
+// 128-byte swizzle), so up to two pages per warp are in flight while it
+// computes on the third. Per page a warp:
+//   * reads K as MMA A-fragments with ldmatrix (16 tokens x 128 dims),
+//   * rotates every key at position start + slot in registers and rounds it to
+//     fp16; the angle's cos/sin come from angle addition, (start) from the page's
+//     row of the fp32 position table (one 512 B row per page, shared by the
+//     lanes) and (slot) from a 16-row copy of the table kept in shared memory,
+//     so the table adds 1/16 of a page's bytes to the L2 traffic,
+//   * computes S^T = K' Q'^T with m16n8k16 MMAs (N = the group's <= 8 heads),
+//   * runs the online softmax in the log2 domain (q is pre-scaled by
 //     log2(e)/sqrt(D)),
-//   * accumulates O^T += V^T P^T with bf16 MMAs (P transposed by movmatrix).
+//   * accumulates O^T += V^T P^T (V^T fragments from ldmatrix.trans, P^T from
+//     movmatrix).
 // Warps combine through shared memory; splits combine through a partial buffer
 // in the workspace, reduced by the last CTA of each (r, h) to arrive (atomic
-// ticket, no waiting).
-//
-// The head dimension's order inside the MMA is a free permutation as long as the
-// K and Q fragments agree; it is chosen so that each lane's 16-byte loads cover
-// whole 32-byte sectors and each rotate-half pair (d, d + 64) sits in one lane.
+// ticket, nobody waits). Every wait on a TMA is bounded; on a timeout the warp
+// drains its copies and the CTA records LAZYATTN_EDEVICE.
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace lazyattn {
 
 namespace {
 
+using namespace tc;
+
 constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 8192;                 // K tile (2 x 2 KB) + V tile (2 x 2 KB)
+constexpr int kSlotRowBytes = 576;              // 64 (cos, sin) + 64 B pad: conflict-free per-lane reads
+constexpr int kSlotTableOff = kWarps * kStages * kStageBytes;
+constexpr int kSmemBytes = kSlotTableOff + kPage * kSlotRowBytes + 1024;
 constexpr int kMaxGroup = 8;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
     const uint64_t* entries;
@@ -56,28 +67,21 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
-__device__ __forceinline__ uint32_t u4get(const uint4& v, int i) {
-    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(static_cast<const uint4*>(p)); }
-__device__ __forceinline__ float4 ldg16f(const void* p) { return __ldg(static_cast<const float4*>(p)); }
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -87,68 +91,49 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
 }
 
-// Lane (gr, c) owns, for its key row, dims {32j + 8c + e : j < 4, e < 8}: four
-// 16-byte chunks. Chunks j and j + 2 hold the rotate-half pairs (d, d + 64).
-// Rotate one row at logical position pos (unless it is already rotated), scale
-// it and emit 16 fp16x2 registers; register 4j + i holds dims (32j + 8c + 2i, +1).
-template <bool PREROT>
-__device__ __forceinline__ void rotate_row(const uint4 (&kc)[4], const float2* __restrict__ rope, int pos, int c,
-                                           float scale, uint32_t (&outr)[16]) {
-    float x[4][8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = u4get(kc[j], i);
-            x[j][2 * i] = bf_lo(w);
-            x[j][2 * i + 1] = bf_hi(w);
-        }
-    }
-    if (!PREROT) {
-        const float2* row = rope + (size_t)pos * (kD / 2);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float* cs = reinterpret_cast<const float*>(row + 32 * j + 8 * c);
-            float t[16];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const float4 f = ldg16f(cs + 4 * v);
-                t[4 * v] = f.x;
-                t[4 * v + 1] = f.y;
-                t[4 * v + 2] = f.z;
-                t[4 * v + 3] = f.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float co = t[2 * e], si = t[2 * e + 1];
-                const float a = x[j][e], b = x[j + 2][e];
-                x[j][e] = a * co - b * si;
-                x[j + 2][e] = a * si + b * co;
-            }
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) outr[4 * j + i] = pack_h2(x[j][2 * i] * scale, x[j][2 * i + 1] * scale);
+// Same predicate in every lane: how many slots of the entry hold keys (0: skip;
+// -1: out-of-range page or positions, also skipped and reported).
+__device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
+    const int n = entry_nvalid(e);
+    if (n == 0) return 0;
+    if (entry_page(e) >= (uint32_t)pv.num_pages || n > kPage || entry_start(e) + n > pv.max_position) return -1;
+    return n;
 }
 
+// Rotate a pair of bf16x2 registers holding dims (d, d+1) and (d+64, d+65) by
+// the angles whose (cos, sin) are cs = (c_d, s_d, c_{d+1}, s_{d+1}); fp16x2 out.
+__device__ __forceinline__ void rotate2(uint32_t& x, uint32_t& y, const float4& cs) {
+    const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
+    x = pack_h2(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w);
+    y = pack_h2(a0 * cs.y + b0 * cs.x, a1 * cs.w + b1 * cs.z);
+}
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) { return pack_h2(bf_lo(x), bf_hi(x)); }
+
 template <bool PREROT>
-__global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(PoolView pv, DecodeParams P) {
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       PoolView pv, DecodeParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_full[kWarps][kStages];
+    __shared__ float sm_m[kWarps][kMaxGroup], sm_l[kWarps][kMaxGroup];
+    __shared__ int s_last, s_abort;
+
     const int s = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gr = lane >> 2, c = lane & 3;
     const int g = P.g, Hq = pv.hq, Hkv = pv.hkv, S = P.splits;
-
-    __shared__ float sm_acc[kWarps][kMaxGroup][kD];
-    __shared__ float sm_m[kWarps][kMaxGroup], sm_l[kWarps][kMaxGroup];
-    __shared__ int s_last;
 
     const int m = P.qpos[r];
     __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
@@ -157,110 +142,193 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(PoolView pv, D
             for (int i = tid; i < g * kD; i += kThreads) out_rh[i] = __float2bfloat16_rn(0.f);
         return;
     }
+    if (tid == 0) s_abort = 0;
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&bar_full[warp][st]), 1);
+        mbar_fence_init();
+    }
+    uint8_t* slot_tab = sm + kSlotTableOff;   // row t: (cos, sin)(t * theta_i), i < 64
+    if (!PREROT) {
+        for (int i = tid; i < kPage * 32; i += kThreads) {
+            const int t = i >> 5, f4 = i & 31;
+            const float4 v = t < pv.max_position ? __ldg(reinterpret_cast<const float4*>(pv.rope) + t * 32 + f4)
+                                                 : make_float4(1.f, 0.f, 1.f, 0.f);
+            *reinterpret_cast<float4*>(slot_tab + t * kSlotRowBytes + f4 * 16) = v;
+        }
+    }
+    __syncthreads();
 
-    // q of head gr of this group, rotated at m, pre-scaled by log2(e)/sqrt(D), as
-    // the B operand (k = head dims, n = head): register 2t / 2t+1 feed k-step t.
-    uint32_t qb[16];
+    // q of head gr, rotated at m and pre-scaled, as the B operand of k-step t:
+    // qb[t][0] = dims (16t+2c, +1), qb[t][1] = dims (16t+2c+8, +9).
+    uint32_t qb[8][2];
     if (gr < g) {
-        const __nv_bfloat16* qp = P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD;
-        uint4 qc[4];
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD);
+        const float4* row = reinterpret_cast<const float4*>(pv.rope + (size_t)m * (kD / 2));
+        const float sc = kLog2e * rsqrtf((float)kD);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) qc[j] = ldg16(qp + 32 * j + 8 * c);
-        rotate_row<false>(qc, pv.rope, m, c, 1.4426950408889634f * rsqrtf((float)kD), qb);
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int d = 16 * t + 2 * c + 8 * hf;
+                const uint32_t x = __ldg(qp + d / 2), y = __ldg(qp + (d + 64) / 2);
+                const float4 cs = __ldg(row + d / 2);
+                const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
+                qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);
+                qb[t + 4][hf] = pack_h2((a0 * cs.y + b0 * cs.x) * sc, (a1 * cs.w + b1 * cs.z) * sc);
+            }
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) qb[i] = 0u;
+        for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
     }
 
     const int e0 = P.entry_offsets[r], e1 = P.entry_offsets[r + 1];
     const int chunk = (e1 - e0 + S - 1) / S;
     const int cb = e0 + s * chunk;
     const int ce = min(e1, cb + chunk);
+    const int n_w = ce - cb > warp ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
+    const uint64_t* my_entries = P.entries + cb + warp;    // page i of this warp: my_entries[kWarps * i]
+    const uint32_t ring = smem_u32(sm + warp * kStages * kStageBytes);
+    volatile int* abort_flag = &s_abort;
 
-    const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(pv.k_pool);
-    const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(pv.v_pool);
+    auto issue = [&](int i) {   // lane 0 only
+        if (i >= n_w) return;
+        const uint64_t e = my_entries[kWarps * i];
+        if (usable_tokens(pv, e) <= 0) return;
+        const int st = i % kStages;
+        const uint32_t bar = smem_u32(&bar_full[warp][st]);
+        const int y = ((int)entry_page(e) * Hkv + h) * kPage;
+        const uint32_t dst = ring + st * kStageBytes;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_2d(dst, &kmap, 0, y, bar);
+        tma_load_2d(dst + 2048, &kmap, 64, y, bar);
+        tma_load_2d(dst + 4096, &vmap, 0, y, bar);
+        tma_load_2d(dst + 6144, &vmap, 64, y, bar);
+    };
+    if (lane == 0)
+        for (int i = 0; i < kStages; ++i) issue(i);
 
     float o[8][4];
 #pragma unroll
     for (int u = 0; u < 8; ++u) o[u][0] = o[u][1] = o[u][2] = o[u][3] = 0.f;
     float mrun0 = -INFINITY, mrun1 = -INFINITY, lrun0 = 0.f, lrun1 = 0.f;
+    uint32_t phases = 0;
+    int consumed_upto = -1;
 
-    const int tok[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    for (int i = 0; i < n_w; ++i) {
+        const uint64_t e = my_entries[kWarps * i];
+        const int nv = usable_tokens(pv, e);
+        const int st = i % kStages;
+        if (nv < 0 && lane == 0) record_error(pv.status, LAZYATTN_ERANGE);
+        if (nv > 0) {
+            if (!mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, abort_flag)) break;
+            phases ^= 1u << st;
+            consumed_upto = i;
+            const int start = entry_start(e);
+            const uint32_t stg = ring + st * kStageBytes;
 
-    for (int ei = cb + warp; ei < ce; ei += kWarps) {
-        const uint64_t e = P.entries[ei];
-        const int nv = entry_nvalid(e);
-        if (nv == 0 || !entry_ok(pv, e)) continue;
-        const int start = entry_start(e);
-        const size_t tile = ((size_t)entry_page(e) * Hkv + h) * kPage * kD;
-        const __nv_bfloat16* kt = kpool + tile;
-        const __nv_bfloat16* vt = vpool + tile;
-
-        uint4 k0[4], k1[4], vv[4][2];
+            float4 csa[8], csb[8];   // (cos, sin) pairs of the lane's frequencies, tokens gr and gr+8
+            if (!PREROT) {
+                // angle of token t = angle(start) + angle(t); both factors from tables
+                const float4* base = reinterpret_cast<const float4*>(pv.rope + (size_t)start * (kD / 2));
+                const float4* sa = reinterpret_cast<const float4*>(slot_tab + gr * kSlotRowBytes);
+                const float4* sb = reinterpret_cast<const float4*>(slot_tab + (gr + 8) * kSlotRowBytes);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            k0[j] = ldg16(kt + gr * kD + 32 * j + 8 * c);
-            k1[j] = ldg16(kt + (gr + 8) * kD + 32 * j + 8 * c);
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int f4 = 8 * t + c + 4 * hf;
+                        const float4 b4 = __ldg(base + f4), x = sa[f4], y = sb[f4];
+                        csa[2 * t + hf] = make_float4(b4.x * x.x - b4.y * x.y, b4.y * x.x + b4.x * x.y,
+                                                      b4.z * x.z - b4.w * x.w, b4.w * x.z + b4.z * x.w);
+                        csb[2 * t + hf] = make_float4(b4.x * y.x - b4.y * y.y, b4.y * y.x + b4.x * y.y,
+                                                      b4.z * y.z - b4.w * y.w, b4.w * y.z + b4.z * y.w);
+                    }
+            }
+            // K as A operand: ka[t] = (tokens gr | gr+8) x (dims 16t+2c.. | 16t+2c+8..)
+            uint32_t ka[8][4];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int row = lane & 15, unit = (t & 3) * 2 + (lane >> 4);
+                ldsm_x4(ka[t], stg + (t >> 2) * 2048 + row * 128 + ((unit ^ (row & 7)) << 4));
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (!PREROT) {
+                    rotate2(ka[t][0], ka[t + 4][0], csa[2 * t]);
+                    rotate2(ka[t][1], ka[t + 4][1], csb[2 * t]);
+                    rotate2(ka[t][2], ka[t + 4][2], csa[2 * t + 1]);
+                    rotate2(ka[t][3], ka[t + 4][3], csb[2 * t + 1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ka[t][j] = bf2_to_h2(ka[t][j]);
+                        ka[t + 4][j] = bf2_to_h2(ka[t + 4][j]);
+                    }
+                }
+            }
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < 8; ++t) mma_f16(sacc, ka[t][0], ka[t][1], ka[t][2], ka[t][3], qb[t][0], qb[t][1]);
+
+            // S^T fragment: (token gr | gr+8) x (head 2c | 2c+1)
+            const bool v0 = gr < nv, v1 = gr + 8 < nv;
+            const float s0 = v0 ? sacc[0] : -INFINITY;
+            const float s1 = v0 ? sacc[1] : -INFINITY;
+            const float s2 = v1 ? sacc[2] : -INFINITY;
+            const float s3 = v1 ? sacc[3] : -INFINITY;
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
+            const float cr0 = fast_exp2(mrun0 - mn0), cr1 = fast_exp2(mrun1 - mn1);
+            const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+            const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+            lrun0 = lrun0 * cr0 + p0 + p2;
+            lrun1 = lrun1 * cr1 + p1 + p3;
+            mrun0 = mn0;
+            mrun1 = mn1;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                o[u][0] *= cr0;
+                o[u][1] *= cr1;
+                o[u][2] *= cr0;
+                o[u][3] *= cr1;
+            }
+            const uint32_t pb0 = movmatrix_t(pack_bf2(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_bf2(p2, p3));
+
+            // V^T as A operand: (dims 16u+gr | 16u+8+gr) x (tokens 2c,2c+1 | 2c+8,2c+9)
+            const int vtok = (lane & 7) + ((lane >> 4) << 3);
+            const uint32_t keep0 = ((2 * c < nv) ? 0x0000ffffu : 0u) | ((2 * c + 1 < nv) ? 0xffff0000u : 0u);
+            const uint32_t keep1 = ((2 * c + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * c + 9 < nv) ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int U = 2 * u + ((lane >> 3) & 1);
+                uint32_t va[4];
+                ldsm_x4_t(va, stg + 4096 + (U >> 3) * 2048 + vtok * 128 + (((U & 7) ^ (vtok & 7)) << 4));
+                // slots past nv never reach the MMA (0 * NaN)
+                mma_bf16(o[u], va[0] & keep0, va[1] & keep0, va[2] & keep1, va[3] & keep1, pb0, pb1);
+            }
         }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            vv[t][0] = ldg16(vt + tok[t] * kD + 8 * gr);
-            vv[t][1] = ldg16(vt + tok[t] * kD + 64 + 8 * gr);
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async_smem();   // this warp's reads of the stage precede the next TMA into it
+            issue(i + kStages);
         }
-
-        // rotate keys at their positions; slots past nv stay in range of the table
-        uint32_t ka0[16], ka1[16];
-        rotate_row<PREROT>(k0, pv.rope, gr < nv ? start + gr : start, c, 1.f, ka0);
-        rotate_row<PREROT>(k1, pv.rope, gr + 8 < nv ? start + gr + 8 : start, c, 1.f, ka1);
-
-        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int t = 0; t < 8; ++t) mma_f16(sacc, ka0[2 * t], ka1[2 * t], ka0[2 * t + 1], ka1[2 * t + 1], qb[2 * t], qb[2 * t + 1]);
-
-        // S^T fragment: (token gr | gr+8) x (head 2c | 2c+1)
-        const bool v0 = gr < nv, v1 = gr + 8 < nv;
-        const float s0 = v0 ? sacc[0] : -INFINITY;
-        const float s1 = v0 ? sacc[1] : -INFINITY;
-        const float s2 = v1 ? sacc[2] : -INFINITY;
-        const float s3 = v1 ? sacc[3] : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
-        const float cr0 = fast_exp2(mrun0 - mn0), cr1 = fast_exp2(mrun1 - mn1);
-        const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-        const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-        lrun0 = lrun0 * cr0 + p0 + p2;
-        lrun1 = lrun1 * cr1 + p1 + p3;
-        mrun0 = mn0;
-        mrun1 = mn1;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            o[u][0] *= cr0;
-            o[u][1] *= cr1;
-            o[u][2] *= cr0;
-            o[u][3] *= cr1;
-        }
-        const uint32_t pb0 = movmatrix_t(pack_bf2(p0, p1));
-        const uint32_t pb1 = movmatrix_t(pack_bf2(p2, p3));
-
-        if (nv < kPage) {   // never let stale slots reach the MMA (0 * NaN)
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                if (tok[t] >= nv) vv[t][0] = vv[t][1] = make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int qi = u >> 1;
-            const uint32_t sel = (u & 1) ? 0x7632u : 0x5410u;
-            const uint32_t a0 = prmt(u4get(vv[0][0], qi), u4get(vv[1][0], qi), sel);
-            const uint32_t a1 = prmt(u4get(vv[0][1], qi), u4get(vv[1][1], qi), sel);
-            const uint32_t a2 = prmt(u4get(vv[2][0], qi), u4get(vv[3][0], qi), sel);
-            const uint32_t a3 = prmt(u4get(vv[2][1], qi), u4get(vv[3][1], qi), sel);
-            mma_bf16(o[u], a0, a1, a2, a3, pb0, pb1);
+    }
+    if (*abort_flag && lane == 0) {
+        // drain copies this warp issued but did not consume before the CTA releases its smem
+        volatile int never = 0;
+        for (int i = consumed_upto + 1; i < min(n_w, consumed_upto + 1 + kStages); ++i) {
+            const uint64_t e = my_entries[kWarps * i];
+            if (usable_tokens(pv, e) <= 0) continue;
+            const int st = i % kStages;
+            mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, &never);
+            phases ^= 1u << st;
         }
     }
 
@@ -269,13 +337,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(PoolView pv, D
         lrun0 += __shfl_xor_sync(0xffffffffu, lrun0, off);
         lrun1 += __shfl_xor_sync(0xffffffffu, lrun1, off);
     }
-    // O^T fragment of m-tile u: dims 8gr+u (c0, c1) and 64+8gr+u (c2, c3); heads 2c, 2c+1
+    __syncthreads();   // every warp is done with its ring: reuse it for the combine
+    float* sm_acc = reinterpret_cast<float*>(sm);   // [kWarps][kMaxGroup][kD]
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        sm_acc[warp][2 * c][8 * gr + u] = o[u][0];
-        sm_acc[warp][2 * c + 1][8 * gr + u] = o[u][1];
-        sm_acc[warp][2 * c][64 + 8 * gr + u] = o[u][2];
-        sm_acc[warp][2 * c + 1][64 + 8 * gr + u] = o[u][3];
+        float* a0 = sm_acc + ((size_t)warp * kMaxGroup + 2 * c) * kD;
+        float* a1 = a0 + kD;
+        a0[16 * u + gr] = o[u][0];
+        a1[16 * u + gr] = o[u][1];
+        a0[16 * u + 8 + gr] = o[u][2];
+        a1[16 * u + 8 + gr] = o[u][3];
     }
     if (gr == 0) {
         sm_m[warp][2 * c] = mrun0;
@@ -284,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(PoolView pv, D
         sm_l[warp][2 * c + 1] = lrun1;
     }
     __syncthreads();
+    if (tid == 0 && s_abort) record_error(pv.status, LAZYATTN_EDEVICE);
 
     // combine the four warps: thread -> (head hh, dims d0 .. d0+7)
     const int hh = tid >> 4, d0 = (tid & 15) * 8;
@@ -298,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(PoolView pv, D
         for (int w = 0; w < kWarps; ++w) {
             const float wt = fast_exp2(sm_m[w][hh] - M);
             L += sm_l[w][hh] * wt;
+            const float* src = sm_acc + ((size_t)w * kMaxGroup + hh) * kD + d0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] += sm_acc[w][hh][d0 + i] * wt;
+            for (int i = 0; i < 8; ++i) a[i] += src[i] * wt;
         }
     }
 
@@ -383,8 +456,13 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 int decode_occupancy(int* ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false>, kThreads, 0) ==
-                   cudaSuccess
+    if (cudaFuncSetAttribute(decode_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+        return LAZYATTN_ECUDA;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false>, kThreads,
+                                                         kSmemBytes) == cudaSuccess
                ? LAZYATTN_OK
                : LAZYATTN_ECUDA;
 }
@@ -405,6 +483,7 @@ DecodeWs decode_ws_layout(const lazyattn_pool& p, const lazyattn_batch& b) {
 
 int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
                        __nv_bfloat16* out, void* ws, const DecodeWs& L, cudaStream_t stream) {
+    if (!p.have_maps) return LAZYATTN_ECUDA;
     char* base = static_cast<char*>(ws);
     DecodeParams P;
     P.entries = b.entries;
@@ -419,9 +498,9 @@ int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __
     P.g = p.d.n_q_heads / p.d.n_kv_heads;
     dim3 grid(L.splits, p.d.n_kv_heads, b.num_requests);
     if (b.flags & LAZYATTN_KEYS_PREROTATED)
-        decode_bf16_kernel<true><<<grid, kThreads, 0, stream>>>(p.view(), P);
+        decode_bf16_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
     else
-        decode_bf16_kernel<false><<<grid, kThreads, 0, stream>>>(p.view(), P);
+        decode_bf16_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }
 

@@ -50,14 +50,22 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
     }
 }
 
-// Find the append slot of request r: first entry with nvalid < 16 in the
-// trailing run of writable entries. Returns the entry index or -1.
-__device__ int find_append_entry(const uint64_t* entries, int e0, int e1) {
+// Find the append slot of request r: the first entry with nvalid < 16 in the
+// trailing run of writable entries. One warp scans 32 entries per step from
+// the end of the request's entries. Returns the entry index or -1 (all lanes).
+__device__ int find_append_entry(const uint64_t* entries, int e0, int e1, int lane) {
     int tail = -1;
-    for (int i = e1 - 1; i >= e0; --i) {
-        const uint64_t e = entries[i];
-        if (!entry_writable(e)) break;
-        if (entry_nvalid(e) < kPage) tail = i;
+    for (int base = e1 - 1; base >= e0; base -= 32) {
+        const int i = base - lane;
+        const bool in = i >= e0;
+        const uint64_t e = in ? entries[i] : 0ull;
+        const bool w = in && entry_writable(e);
+        const unsigned brk = __ballot_sync(0xffffffffu, !w);            // run ends at the first such lane
+        const int stop = brk ? __ffs(brk) - 1 : 32;
+        unsigned cand = __ballot_sync(0xffffffffu, w && entry_nvalid(e) < kPage);
+        if (stop < 32) cand &= (1u << stop) - 1u;
+        if (cand) tail = base - (31 - __clz(cand));                     // furthest back = first in table order
+        if (stop < 32) break;
     }
     return tail;
 }
@@ -69,22 +77,24 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
     const int r = blockIdx.x;
     __shared__ int s_entry;
     __shared__ uint64_t s_e;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
         const int e0 = entry_offsets[r], e1 = entry_offsets[r + 1];
-        int t = find_append_entry(entries, e0, e1);
-        if (t >= 0) {
-            const uint64_t e = entries[t];
-            const int32_t pos = entry_start(e) + entry_nvalid(e);
-            if (entry_page(e) >= (uint32_t)pv.num_pages || pos >= pv.max_position) {
-                record_error(pv.status, LAZYATTN_ERANGE);
-                t = -1;
+        int t = find_append_entry(entries, e0, e1, threadIdx.x);
+        if (threadIdx.x == 0) {
+            if (t >= 0) {
+                const uint64_t e = entries[t];
+                const int32_t pos = entry_start(e) + entry_nvalid(e);
+                if (entry_page(e) >= (uint32_t)pv.num_pages || pos >= pv.max_position) {
+                    record_error(pv.status, LAZYATTN_ERANGE);
+                    t = -1;
+                }
+            } else {
+                record_error(pv.status, LAZYATTN_ENODECODE);
             }
-        } else {
-            record_error(pv.status, LAZYATTN_ENODECODE);
+            s_entry = t;
+            s_e = t >= 0 ? entries[t] : 0;
+            qpos[r] = t >= 0 ? entry_start(s_e) + entry_nvalid(s_e) : -1;
         }
-        s_entry = t;
-        s_e = t >= 0 ? entries[t] : 0;
-        qpos[r] = t >= 0 ? entry_start(s_e) + entry_nvalid(s_e) : -1;
     }
     __syncthreads();
     if (s_entry < 0) return;

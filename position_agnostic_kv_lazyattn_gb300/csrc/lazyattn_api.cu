@@ -88,11 +88,15 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         return LAZYATTN_ECUDA;
     }
     int occ = 1;
-    if (d.dtype == LAZYATTN_BF16 && decode_occupancy(&occ) != LAZYATTN_OK) {
+    if (d.dtype == LAZYATTN_BF16 && (decode_occupancy(&occ) != LAZYATTN_OK || prefill_init() != LAZYATTN_OK)) {
         delete p;
         return LAZYATTN_ECUDA;
     }
     p->decode_slots = p->sm_count * std::max(occ, 1);
+    if (d.dtype == LAZYATTN_BF16 && !encode_pool_maps(*p)) {
+        delete p;
+        return LAZYATTN_EINVAL;   // pool too large for 32-bit TMA rows, or no tensor-map support
+    }
 
     // Position table: angle pos * theta^(-2i/D) in fp64, cos/sin in fp64, stored fp32.
     const int half = d.head_dim / 2;

@@ -1,0 +1,49 @@
+// Host-side construction of the TMA tensor maps over a pool's K and V buffers.
+#include <cudaTypedefs.h>
+#include <limits.h>
+
+#include "internal.h"
+
+namespace lazyattn {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode_one(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t rows, int d) {
+    cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_pool_maps(lazyattn_pool& p) {
+    p.have_maps = false;
+    if (p.d.dtype != LAZYATTN_BF16) return false;
+    const uint64_t rows = (uint64_t)p.d.num_pages * (uint64_t)p.d.n_kv_heads * kPage;
+    if (rows + kPage > (uint64_t)INT_MAX) return false;
+    auto enc = get_encoder();
+    if (!enc) return false;
+    if (!encode_one(enc, &p.kmap, p.d.k_pool, rows, p.d.head_dim)) return false;
+    if (!encode_one(enc, &p.vmap, p.d.v_pool, rows, p.d.head_dim)) return false;
+    p.have_maps = true;
+    return true;
+}
+
+}  // namespace lazyattn
