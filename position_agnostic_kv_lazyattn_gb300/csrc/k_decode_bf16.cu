@@ -5,10 +5,10 @@
 //
 // Work split: a CTA owns (request r, KV head h, split s) and a contiguous run of
 // the request's pages; its four warps take the run's pages round-robin. Each
-// warp keeps its own ring of three page stages in shared memory, filled by TMA
+// warp keeps its own ring of two page stages in shared memory, filled by TMA
 // (lane 0 issues; K and V tiles of one page are 4 KB each, two 64-dim boxes with
-// 128-byte swizzle), so up to two pages per warp are in flight while it
-// computes on the third. Per page a warp:
+// 128-byte swizzle), so the next page is in flight while it computes on the
+// current one; three CTAs (12 warps) share an SM. Per page a warp:
 //   * reads K as MMA A-fragments with ldmatrix (16 tokens x 128 dims),
 //   * rotates every key at position start + slot in registers and rounds it to
 //     fp16; the angle's cos/sin come from angle addition, (start) from the page's
@@ -36,7 +36,7 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kStageBytes = 8192;                 // K tile (2 x 2 KB) + V tile (2 x 2 KB)
 constexpr int kSlotRowBytes = 576;              // 64 (cos, sin) + 64 B pad: conflict-free per-lane reads
 constexpr int kSlotTableOff = kWarps * kStages * kStageBytes;
@@ -121,7 +121,7 @@ __device__ __forceinline__ void rotate2(uint32_t& x, uint32_t& y, const float4& 
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) { return pack_h2(bf_lo(x), bf_hi(x)); }
 
 template <bool PREROT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        PoolView pv, DecodeParams P) {
     extern __shared__ uint8_t smem_raw[];
@@ -227,49 +227,42 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int start = entry_start(e);
             const uint32_t stg = ring + st * kStageBytes;
 
-            float4 csa[8], csb[8];   // (cos, sin) pairs of the lane's frequencies, tokens gr and gr+8
-            if (!PREROT) {
-                // angle of token t = angle(start) + angle(t); both factors from tables
-                const float4* base = reinterpret_cast<const float4*>(pv.rope + (size_t)start * (kD / 2));
-                const float4* sa = reinterpret_cast<const float4*>(slot_tab + gr * kSlotRowBytes);
-                const float4* sb = reinterpret_cast<const float4*>(slot_tab + (gr + 8) * kSlotRowBytes);
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int f4 = 8 * t + c + 4 * hf;
-                        const float4 b4 = __ldg(base + f4), x = sa[f4], y = sb[f4];
-                        csa[2 * t + hf] = make_float4(b4.x * x.x - b4.y * x.y, b4.y * x.x + b4.x * x.y,
-                                                      b4.z * x.z - b4.w * x.w, b4.w * x.z + b4.z * x.w);
-                        csb[2 * t + hf] = make_float4(b4.x * y.x - b4.y * y.y, b4.y * y.x + b4.x * y.y,
-                                                      b4.z * y.z - b4.w * y.w, b4.w * y.z + b4.z * y.w);
-                    }
-            }
-            // K as A operand: ka[t] = (tokens gr | gr+8) x (dims 16t+2c.. | 16t+2c+8..)
-            uint32_t ka[8][4];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int row = lane & 15, unit = (t & 3) * 2 + (lane >> 4);
-                ldsm_x4(ka[t], stg + (t >> 2) * 2048 + row * 128 + ((unit ^ (row & 7)) << 4));
-            }
+            // K' = rotated keys as the A operand; k-steps t and t+4 hold the rotate-half
+            // partners (dims 16t+.. and 64+16t+..), so they are loaded, rotated and
+            // multiplied together: (tokens gr | gr+8) x (dims 16t+2c.. | 16t+2c+8..)
+            const float4* base = reinterpret_cast<const float4*>(pv.rope + (size_t)start * (kD / 2));
+            const float4* sa = reinterpret_cast<const float4*>(slot_tab + gr * kSlotRowBytes);
+            const float4* sb = reinterpret_cast<const float4*>(slot_tab + (gr + 8) * kSlotRowBytes);
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
+                uint32_t lo[4], hi[4];
+                const int row = lane & 15, unit = (t & 3) * 2 + (lane >> 4);
+                ldsm_x4(lo, stg + row * 128 + ((unit ^ (row & 7)) << 4));
+                ldsm_x4(hi, stg + 2048 + row * 128 + ((unit ^ (row & 7)) << 4));
                 if (!PREROT) {
-                    rotate2(ka[t][0], ka[t + 4][0], csa[2 * t]);
-                    rotate2(ka[t][1], ka[t + 4][1], csb[2 * t]);
-                    rotate2(ka[t][2], ka[t + 4][2], csa[2 * t + 1]);
-                    rotate2(ka[t][3], ka[t + 4][3], csb[2 * t + 1]);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        // angle of token t = angle(start) + angle(t); both factors from tables
+                        const int f4 = 8 * t + c + 4 * hf;
+                        const float4 b4 = __ldg(base + f4), x = sa[f4], y = sb[f4];
+                        const float4 ca = make_float4(b4.x * x.x - b4.y * x.y, b4.y * x.x + b4.x * x.y,
+                                                      b4.z * x.z - b4.w * x.w, b4.w * x.z + b4.z * x.w);
+                        const float4 cb = make_float4(b4.x * y.x - b4.y * y.y, b4.y * y.x + b4.x * y.y,
+                                                      b4.z * y.z - b4.w * y.w, b4.w * y.z + b4.z * y.w);
+                        rotate2(lo[2 * hf], hi[2 * hf], ca);
+                        rotate2(lo[2 * hf + 1], hi[2 * hf + 1], cb);
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        ka[t][j] = bf2_to_h2(ka[t][j]);
-                        ka[t + 4][j] = bf2_to_h2(ka[t + 4][j]);
+                        lo[j] = bf2_to_h2(lo[j]);
+                        hi[j] = bf2_to_h2(hi[j]);
                     }
                 }
+                mma_f16(sacc, lo[0], lo[1], lo[2], lo[3], qb[t][0], qb[t][1]);
+                mma_f16(sacc, hi[0], hi[1], hi[2], hi[3], qb[t + 4][0], qb[t + 4][1]);
             }
-            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int t = 0; t < 8; ++t) mma_f16(sacc, ka[t][0], ka[t][1], ka[t][2], ka[t][3], qb[t][0], qb[t][1]);
 
             // S^T fragment: (token gr | gr+8) x (head 2c | 2c+1)
             const bool v0 = gr < nv, v1 = gr + 8 < nv;
@@ -291,27 +284,38 @@ __global__ void __launch_bounds__(kThreads, 2)
             lrun1 = lrun1 * cr1 + p1 + p3;
             mrun0 = mn0;
             mrun1 = mn1;
+            if (__any_sync(0xffffffffu, cr0 != 1.f || cr1 != 1.f)) {   // rescale only when a max moved
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                o[u][0] *= cr0;
-                o[u][1] *= cr1;
-                o[u][2] *= cr0;
-                o[u][3] *= cr1;
+                for (int u = 0; u < 8; ++u) {
+                    o[u][0] *= cr0;
+                    o[u][1] *= cr1;
+                    o[u][2] *= cr0;
+                    o[u][3] *= cr1;
+                }
             }
             const uint32_t pb0 = movmatrix_t(pack_bf2(p0, p1));
             const uint32_t pb1 = movmatrix_t(pack_bf2(p2, p3));
 
             // V^T as A operand: (dims 16u+gr | 16u+8+gr) x (tokens 2c,2c+1 | 2c+8,2c+9)
             const int vtok = (lane & 7) + ((lane >> 4) << 3);
-            const uint32_t keep0 = ((2 * c < nv) ? 0x0000ffffu : 0u) | ((2 * c + 1 < nv) ? 0xffff0000u : 0u);
-            const uint32_t keep1 = ((2 * c + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * c + 9 < nv) ? 0xffff0000u : 0u);
+            if (nv == kPage) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int U = 2 * u + ((lane >> 3) & 1);
-                uint32_t va[4];
-                ldsm_x4_t(va, stg + 4096 + (U >> 3) * 2048 + vtok * 128 + (((U & 7) ^ (vtok & 7)) << 4));
-                // slots past nv never reach the MMA (0 * NaN)
-                mma_bf16(o[u], va[0] & keep0, va[1] & keep0, va[2] & keep1, va[3] & keep1, pb0, pb1);
+                for (int u = 0; u < 8; ++u) {
+                    const int U = 2 * u + ((lane >> 3) & 1);
+                    uint32_t va[4];
+                    ldsm_x4_t(va, stg + 4096 + (U >> 3) * 2048 + vtok * 128 + (((U & 7) ^ (vtok & 7)) << 4));
+                    mma_bf16(o[u], va[0], va[1], va[2], va[3], pb0, pb1);
+                }
+            } else {   // slots past nv never reach the MMA (0 * NaN)
+                const uint32_t keep0 = ((2 * c < nv) ? 0x0000ffffu : 0u) | ((2 * c + 1 < nv) ? 0xffff0000u : 0u);
+                const uint32_t keep1 = ((2 * c + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * c + 9 < nv) ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int U = 2 * u + ((lane >> 3) & 1);
+                    uint32_t va[4];
+                    ldsm_x4_t(va, stg + 4096 + (U >> 3) * 2048 + vtok * 128 + (((U & 7) ^ (vtok & 7)) << 4));
+                    mma_bf16(o[u], va[0] & keep0, va[1] & keep0, va[2] & keep1, va[3] & keep1, pb0, pb1);
+                }
             }
         }
         __syncwarp();
