@@ -11,9 +11,9 @@
 // (query token, query head of the group) pair, so every K/V tile and its
 // rotation serve 256 rows of the group. Tiles of 64 keys (4 pages) stream
 // through a 3-stage ring. Roles (16 warps = 4 warpgroups):
-//   warp 0        TMA producer: per tile 4 pages x (K, V) x two 64-dim boxes
-//                 (128B swizzle) plus each page's row (cos, sin)(start * theta)
-//                 of the position table (bulk copy)
+//   warps 0, 2    TMA producers, K ring and V ring: per tile 4 pages x two
+//                 64-dim boxes (128B swizzle); with K, each page's row
+//                 (cos, sin)(start * theta) of the position table (bulk copy)
 //   warp 1        TMEM owner and single-thread UMMA issuer, per tile:
 //                 S_i = Q_i K^T (fp16, 128x64x128) for both Q tiles, then
 //                 O_i += P_i V of the previous tile (bf16, 128x128x64)
@@ -27,7 +27,11 @@
 //                 in shared memory; written back in place as fp16
 // S is double-buffered per Q tile in TMEM (4 x 64 columns) next to O (2 x 128).
 // Tiles whose keys are all masked for every row of the CTA (past the causal
-// edge, or empty entries) are skipped by every role alike. Every wait is
+// edge, or empty entries) are skipped. Only the producer reads the block
+// table: with each stage it publishes the tile's page starts and token counts
+// in shared memory (before arriving on the stage's barrier), and after the last
+// tile a sentinel stage, so the consumer roles never touch global memory inside
+// the tile loop. Every wait is
 // bounded; a timeout raises an abort flag that all roles honour, drains
 // in-flight copies and MMAs, frees TMEM and records LAZYATTN_EDEVICE.
 #include <limits.h>
@@ -71,6 +75,13 @@ constexpr float kRescaleThreshold = 8.0f;          // log2 units
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
+// What the producer tells the consumers about the tile in a stage.
+struct TileInfo {
+    int j;                        // tile index, -1: no more tiles
+    int start[kPagesPerTile];     // logical position of slot 0 of each page
+    int n[kPagesPerTile];         // keys in each page (0: none / unusable)
+};
+
 struct PrefillParams {
     const uint64_t* entries;
     const int32_t* entry_offsets;
@@ -97,6 +108,21 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+// 2^x on the FMA pipe, to share the softmax's exponentials with the MUFU pipe.
+// Cody-Waite style range reduction: x = n + f with n = round(x) (the 1.5 * 2^23
+// shift leaves n in the low mantissa bits of t) and f in [-0.5, 0.5]; 2^f from a
+// degree-3 polynomial fitted here by least squares on Chebyshev nodes (maximum
+// relative error 7.5e-5, far below the bf16 rounding of P); n is added to the
+// exponent field. Returns exactly 0 below 2^-126 (masked keys give -inf).
+__device__ __forceinline__ float exp2_poly(float x) {
+    const float xc = fmaxf(x, -126.f);
+    const float t = xc + 12582912.f;
+    const float n = t - 12582912.f;
+    const float f = xc - n;
+    const float p = fmaf(fmaf(fmaf(0.0551716648f, f, 0.242611125f), f, 0.693260968f), f, 0.999928057f);
+    const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+    return x < -126.f ? 0.f : r;
 }
 __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
     x[0] = bf_lo(v.x); x[1] = bf_hi(v.x); x[2] = bf_lo(v.y); x[3] = bf_hi(v.y);
@@ -138,9 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_kready[kStages];
+    __shared__ uint64_t bar_kfull[kStages], bar_kempty[kStages], bar_vfull[kStages], bar_vempty[kStages];
+    __shared__ uint64_t bar_kready[kStages];
     __shared__ uint64_t bar_sfull[kQTiles][2], bar_sfree[kQTiles][2], bar_pfull[kQTiles], bar_odone[kQTiles];
     __shared__ uint64_t bar_qready, bar_drain;
+    __shared__ TileInfo s_info[kStages];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -166,8 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+            mbar_init(smem_u32(&bar_kfull[s]), 1);
+            mbar_init(smem_u32(&bar_kempty[s]), 1);
+            mbar_init(smem_u32(&bar_vfull[s]), 1);
+            mbar_init(smem_u32(&bar_vempty[s]), 1);
             mbar_init(smem_u32(&bar_kready[s]), 128);
         }
         for (int i = 0; i < kQTiles; ++i) {
@@ -192,46 +222,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ TMA producers
+        // Warp 0 streams K tiles (with the pages' position-table rows and the
+        // tile info), warp 2 streams V tiles, each through its own ring: a K
+        // stage is reused once the tile's QK MMAs are done, a V stage once its PV
+        // MMAs are, so both loads are requested several tiles ahead.
+        const bool is_k = warp == 0;
         if (lane == 0 && T > 0) {
+            uint64_t* full = is_k ? bar_kfull : bar_vfull;
+            uint64_t* empty = is_k ? bar_kempty : bar_vempty;
+            const CUtensorMap* map = is_k ? &kmap : &vmap;
+            const int off = is_k ? kOffK : kOffV;
             int last_k[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s) last_k[s] = -1;
             int k = 0;
-            for (int j = 0; j < T; ++j) {
-                if (!tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
+            bool ok = true;
+            for (int j = 0; j <= T; ++j) {
+                if (j < T && !tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
+                if (j == T && !is_k) break;
                 const int st = k % kStages;
-                if (k >= kStages && !mbar_wait(smem_u32(&bar_empty[st]), ((k / kStages) - 1) & 1, abort_flag)) break;
-                const uint32_t fb = smem_u32(&bar_full[st]);
-                mbar_arrive_expect_tx(fb, 2 * kKVBytes + kBaseBytes);
-                const uint32_t ks = smem_u32(sm + kOffK + st * kKVBytes);
-                const uint32_t vs = smem_u32(sm + kOffV + st * kKVBytes);
+                if (k >= kStages && !mbar_wait(smem_u32(&empty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full[st]);
+                TileInfo& info = s_info[st];
+                if (j == T) {   // sentinel: no more tiles
+                    info.j = -1;
+                    mbar_arrive(fb);
+                    break;
+                }
+                const uint32_t ds = smem_u32(sm + off + st * kKVBytes);
                 const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
+                int ys[kPagesPerTile];
+                const float2* bases[kPagesPerTile];
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     const int idx = e0 + j * kPagesPerTile + p;
-                    int y = P.oob_row;
+                    int y = P.oob_row, n = 0, st0 = 0;
                     const float2* base = pv.rope;
                     if (idx < e1) {
                         const uint64_t e = P.entries[idx];
-                        if (usable_tokens(pv, e) > 0) {
+                        n = usable_tokens(pv, e);
+                        st0 = entry_start(e);
+                        if (n < 0 && is_k) record_error(pv.status, LAZYATTN_ERANGE);
+                        if (n > 0) {
                             y = ((int)entry_page(e) * Hkv + h) * kPage;
-                            base = pv.rope + (size_t)entry_start(e) * (kD / 2);
+                            base = pv.rope + (size_t)st0 * (kD / 2);
                         }
                     }
-                    tma_load_2d(ks + p * 2048, &kmap, 0, y, fb);
-                    tma_load_2d(ks + kKVChunk + p * 2048, &kmap, 64, y, fb);
-                    tma_load_2d(vs + p * 2048, &vmap, 0, y, fb);
-                    tma_load_2d(vs + kKVChunk + p * 2048, &vmap, 64, y, fb);
-                    bulk_load(bs + p * 512, base, 512, fb);
+                    if (is_k) {
+                        info.start[p] = st0;
+                        info.n[p] = max(n, 0);
+                    }
+                    ys[p] = y;
+                    bases[p] = base;
+                }
+                if (is_k) info.j = j;
+                // arrive before the copies: releases the info writes to the waiters
+                mbar_arrive_expect_tx(fb, is_k ? kKVBytes + kBaseBytes : kKVBytes);
+                for (int p = 0; p < kPagesPerTile; ++p) {
+                    tma_load_2d(ds + p * 2048, map, 0, ys[p], fb);
+                    tma_load_2d(ds + kKVChunk + p * 2048, map, 64, ys[p], fb);
+                    if (is_k) bulk_load(bs + p * 512, bases[p], 512, fb);
                 }
                 last_k[st] = k;
                 ++k;
             }
+            if (!ok) *abort_flag = 1;
             if (*abort_flag) {   // let issued copies land before the CTA's smem is released
                 volatile int never = 0;
                 for (int s = 0; s < kStages; ++s)
-                    if (last_k[s] >= 0) mbar_wait(smem_u32(&bar_full[s]), (last_k[s] / kStages) & 1, &never);
+                    if (last_k[s] >= 0) mbar_wait(smem_u32(&full[s]), (last_k[s] / kStages) & 1, &never);
             }
         }
     } else if (warp == 1) {
@@ -242,9 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = tile1 ? 2 : 1;
             bool ok = T > 0 && mbar_wait(smem_u32(&bar_qready), 0, abort_flag);
             int k = 0;
-            for (int j = 0; ok && j < T; ++j) {
-                if (!tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
+            for (; ok;) {
                 const int st = k % kStages, b = k & 1;
+                ok = mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag);
+                if (!ok || s_info[st].j < 0) break;
                 ok = mbar_wait(smem_u32(&bar_kready[st]), (k / kStages) & 1, abort_flag);
                 if (!ok) break;
                 const uint32_t ka = smem_u32(sm + kOffK + st * kKVBytes);
@@ -262,9 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(smem_u32(&bar_sfull[i][b]));
                 }
                 if (!ok) break;
+                umma_commit(smem_u32(&bar_kempty[st]));   // K stage free once these QK MMAs finish
                 if (k >= 1) {   // P V of the previous tile
                     const int pst = (k - 1) % kStages;
                     const uint32_t va = smem_u32(sm + kOffV + pst * kKVBytes);
+                    ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
                     for (int i = 0; ok && i < nt; ++i) {
                         ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
                         if (!ok) break;
@@ -278,13 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_commit(smem_u32(&bar_odone[i]));
                     }
                     if (!ok) break;
-                    umma_commit(smem_u32(&bar_empty[pst]));
+                    umma_commit(smem_u32(&bar_vempty[pst]));
                 }
                 ++k;
             }
             if (ok && k >= 1) {   // P V of the last tile
                 const int pst = (k - 1) % kStages;
                 const uint32_t va = smem_u32(sm + kOffV + pst * kKVBytes);
+                ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
                 for (int i = 0; ok && i < nt; ++i) {
                     ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
                     if (!ok) break;
@@ -297,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     umma_commit(smem_u32(&bar_odone[i]));
                 }
-                umma_commit(smem_u32(&bar_empty[pst]));
+                umma_commit(smem_u32(&bar_vempty[pst]));
             }
             // every issued MMA has finished before TMEM / smem are released
             umma_commit(smem_u32(&bar_drain));
@@ -317,19 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");   // slot table complete (rotation warps only)
         const int kr = rt >> 1, hf = rt & 1;              // key row of the tile, half of its units
         const int slot = kr & 15;
-        int k = 0;
-        for (int j = 0; j < T; ++j) {
-            if (!tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
+        for (int k = 0; T > 0; ++k) {
             const int st = k % kStages;
-            if (!mbar_wait(smem_u32(&bar_full[st]), (k / kStages) & 1, abort_flag)) break;
-            const int idx = e0 + j * kPagesPerTile + (kr >> 4);
-            bool valid = false;
-            if (idx < e1) {
-                const uint64_t e = P.entries[idx];
-                const int n = usable_tokens(pv, e);
-                if (n < 0 && slot == 0 && hf == 0) record_error(pv.status, LAZYATTN_ERANGE);
-                valid = slot < n;
-            }
+            if (!mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag)) break;
+            const TileInfo& info = s_info[st];
+            if (info.j < 0) break;
+            const bool valid = slot < info.n[kr >> 4];
+            bool partial = false;   // a page with some, but not all, slots holding keys
+#pragma unroll
+            for (int p = 0; p < kPagesPerTile; ++p) partial = partial || (info.n[p] > 0 && info.n[p] < kPage);
             uint8_t* kb = sm + kOffK + st * kKVBytes;
             uint8_t* vb = sm + kOffV + st * kKVBytes;
             if (valid) {
@@ -359,20 +422,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *p1 = pack8_h(x1);
                     *p2 = pack8_h(x2);
                 }
-            } else {   // no key in this slot: zero K (finite scores) and V (no 0 * NaN)
+            } else {   // no key in this slot: zero K so that its scores stay finite
                 const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     const int u = 4 * hf + uu;
                     *reinterpret_cast<uint4*>(kb + sw128_offset(kr, u)) = z;
                     *reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u)) = z;
-                    *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = z;
-                    *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = z;
+                }
+            }
+            if (partial) {   // stale slots of a partly filled page: zero V too (0 * NaN would be NaN)
+                if (!mbar_wait(smem_u32(&bar_vfull[st]), (k / kStages) & 1, abort_flag)) break;
+                if (!valid) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const int u = 4 * hf + uu;
+                        *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = z;
+                        *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = z;
+                    }
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_kready[st]));
-            ++k;
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax rows
@@ -427,24 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int k = 0;
-        for (int j = 0; active && j < T; ++j) {
-            if (!tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
-            const int b = k & 1;
+        for (; active && T > 0; ++k) {
+            const int st = k % kStages, b = k & 1;
+            ok = mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag);
+            if (!ok) break;
+            const TileInfo& info = s_info[st];
+            if (info.j < 0) break;
             // which keys of the tile this row may see
             int kstart[kPagesPerTile], kn[kPagesPerTile];
             bool full = row_valid;
 #pragma unroll
             for (int p = 0; p < kPagesPerTile; ++p) {
-                const int idx = e0 + j * kPagesPerTile + p;
-                int n = 0, s0 = 0;
-                if (idx < e1) {
-                    const uint64_t e = P.entries[idx];
-                    n = max(usable_tokens(pv, e), 0);
-                    s0 = entry_start(e);
-                }
-                kstart[p] = s0;
-                kn[p] = n;
-                full = full && (n == kPage) && (s0 + kPage - 1 <= m_row);
+                kstart[p] = info.start[p];
+                kn[p] = info.n[p];
+                full = full && (kn[p] == kPage) && (kstart[p] + kPage - 1 <= m_row);
             }
             ok = mbar_wait(smem_u32(&bar_sfull[qi][b]), (k >> 1) & 1, abort_flag);
             if (!ok) break;
@@ -467,23 +535,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s[kk] = vis ? s[kk] : -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            float mx8[8];   // eight independent chains instead of one 64-long one
 #pragma unroll
-            for (int kk = 0; kk < kN; ++kk) mx = fmaxf(mx, s[kk]);
+            for (int kk = 0; kk < 8; ++kk) mx8[kk] = s[kk];
+#pragma unroll
+            for (int kk = 8; kk < kN; ++kk) mx8[kk & 7] = fmaxf(mx8[kk & 7], s[kk]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             float alpha = 1.f;
             if (mx > m_run + kRescaleThreshold) {
                 alpha = fast_exp2(m_run - mx);   // 0 when m_run is -inf
                 m_run = mx;
             }
             const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-            float sum = 0.f;
+            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[kN / 2];
 #pragma unroll
             for (int kk = 0; kk < kN; kk += 2) {
                 const float p0 = fast_exp2(s[kk] - mref), p1 = fast_exp2(s[kk + 1] - mref);
-                sum += p0 + p1;
+                sum8[(kk >> 1) & 7] += p0 + p1;
                 pk[kk / 2] = pack_bf2(p0, p1);
             }
+            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l_run = l_run * alpha + sum;
             if (k >= 1) {
                 ok = mbar_wait(smem_u32(&bar_odone[qi]), (k - 1) & 1, abort_flag);
@@ -509,7 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_pfull[qi]));
-            ++k;
         }
 
         // epilogue: O / l -> bf16 rows of out
