@@ -109,21 +109,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// 2^x on the FMA pipe, to share the softmax's exponentials with the MUFU pipe.
-// Cody-Waite style range reduction: x = n + f with n = round(x) (the 1.5 * 2^23
-// shift leaves n in the low mantissa bits of t) and f in [-0.5, 0.5]; 2^f from a
-// degree-3 polynomial fitted here by least squares on Chebyshev nodes (maximum
-// relative error 7.5e-5, far below the bf16 rounding of P); n is added to the
-// exponent field. Returns exactly 0 below 2^-126 (masked keys give -inf).
-__device__ __forceinline__ float exp2_poly(float x) {
-    const float xc = fmaxf(x, -126.f);
-    const float t = xc + 12582912.f;
-    const float n = t - 12582912.f;
-    const float f = xc - n;
-    const float p = fmaf(fmaf(fmaf(0.0551716648f, f, 0.242611125f), f, 0.693260968f), f, 0.999928057f);
-    const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-    return x < -126.f ? 0.f : r;
-}
 __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
     x[0] = bf_lo(v.x); x[1] = bf_hi(v.x); x[2] = bf_lo(v.y); x[3] = bf_hi(v.y);
     x[4] = bf_lo(v.z); x[5] = bf_hi(v.z); x[6] = bf_lo(v.w); x[7] = bf_hi(v.w);
@@ -303,6 +288,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idqk = idesc_f16(kTileM, kN, 0, 0, 0);
             const uint32_t idpv = idesc_f16(kTileM, kD, 1, 1, 1);
             const int nt = tile1 ? 2 : 1;
+            // Descriptors are built once; a k-step only moves the start address,
+            // i.e. adds (byte offset >> 4) to the low field of the descriptor.
+            // Q tiles, P tiles and ring stages are evenly spaced: index * stride.
+            const uint64_t dq0 = sdesc_sw128(smem_u32(sm + kOffQ), 16, 1024);
+            const uint64_t dp0 = sdesc_sw128(smem_u32(sm + kOffP), 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(sm + kOffV), kKVChunk, 1024);
+            auto issue_qk = [&](int i, int st, int b) {
+                const uint64_t a0 = dq0 + (uint64_t)(i * (kQBytes >> 4)), b0 = dk0 + (uint64_t)(st * (kKVBytes >> 4));
+                const uint32_t d = tmem + i * 128 + b * kN;
+#pragma unroll
+                for (int t = 0; t < kD / 16; ++t) {
+                    const uint64_t oa = (uint64_t)(((t >> 2) * kQChunk + (t & 3) * 32) >> 4);
+                    const uint64_t ob = (uint64_t)(((t >> 2) * kKVChunk + (t & 3) * 32) >> 4);
+                    umma_f16(d, a0 + oa, b0 + ob, idqk, t > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int i, int st, uint32_t first) {
+                const uint64_t a0 = dp0 + (uint64_t)(i * (kPBytes >> 4)), b0 = dv0 + (uint64_t)(st * (kKVBytes >> 4));
+                const uint32_t d = tmem + 256 + i * 128;
+#pragma unroll
+                for (int t = 0; t < kN / 16; ++t)
+                    umma_f16(d, a0 + (uint64_t)(t * 2), b0 + (uint64_t)(t * 128), idpv, (t > 0 || !first) ? 1u : 0u);
+            };
             bool ok = T > 0 && mbar_wait(smem_u32(&bar_qready), 0, abort_flag);
             int k = 0;
             for (; ok;) {
@@ -311,36 +320,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok || s_info[st].j < 0) break;
                 ok = mbar_wait(smem_u32(&bar_kready[st]), (k / kStages) & 1, abort_flag);
                 if (!ok) break;
-                const uint32_t ka = smem_u32(sm + kOffK + st * kKVBytes);
                 for (int i = 0; ok && i < nt; ++i) {
                     if (k >= 2) ok = mbar_wait(smem_u32(&bar_sfree[i][b]), ((k >> 1) - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t qa = smem_u32(sm + kOffQ + i * kQBytes);
-#pragma unroll
-                    for (int t = 0; t < kD / 16; ++t) {
-                        umma_f16(tmem + i * 128 + b * kN,
-                                 sdesc_sw128(qa + (t >> 2) * kQChunk + (t & 3) * 32, 16, 1024),
-                                 sdesc_sw128(ka + (t >> 2) * kKVChunk + (t & 3) * 32, 16, 1024), idqk, t > 0);
-                    }
+                    issue_qk(i, st, b);
                     umma_commit(smem_u32(&bar_sfull[i][b]));
                 }
                 if (!ok) break;
                 umma_commit(smem_u32(&bar_kempty[st]));   // K stage free once these QK MMAs finish
                 if (k >= 1) {   // P V of the previous tile
                     const int pst = (k - 1) % kStages;
-                    const uint32_t va = smem_u32(sm + kOffV + pst * kKVBytes);
                     ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
                     for (int i = 0; ok && i < nt; ++i) {
                         ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t pa = smem_u32(sm + kOffP + i * kPBytes);
-#pragma unroll
-                        for (int t = 0; t < kN / 16; ++t) {
-                            umma_f16(tmem + 256 + i * 128, sdesc_sw128(pa + t * 32, 16, 1024),
-                                     sdesc_sw128(va + t * 2048, kKVChunk, 1024), idpv, (k > 1 || t > 0) ? 1u : 0u);
-                        }
+                        issue_pv(i, pst, k == 1);
                         umma_commit(smem_u32(&bar_odone[i]));
                     }
                     if (!ok) break;
@@ -350,18 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok && k >= 1) {   // P V of the last tile
                 const int pst = (k - 1) % kStages;
-                const uint32_t va = smem_u32(sm + kOffV + pst * kKVBytes);
                 ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
                 for (int i = 0; ok && i < nt; ++i) {
                     ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t pa = smem_u32(sm + kOffP + i * kPBytes);
-#pragma unroll
-                    for (int t = 0; t < kN / 16; ++t) {
-                        umma_f16(tmem + 256 + i * 128, sdesc_sw128(pa + t * 32, 16, 1024),
-                                 sdesc_sw128(va + t * 2048, kKVChunk, 1024), idpv, (k > 1 || t > 0) ? 1u : 0u);
-                    }
+                    issue_pv(i, pst, k == 1);
                     umma_commit(smem_u32(&bar_odone[i]));
                 }
                 umma_commit(smem_u32(&bar_vempty[pst]));

@@ -39,14 +39,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of a barrier, giving up after ~kWaitCycles or when
 // another role raised *abort. Returns false on give-up (and raises *abort).
+// Waiting threads sleep between checks, so they take no issue slots or
+// shared-memory bandwidth from the working roles.
 constexpr long long kWaitCycles = 2000000000ll;   // ~1 s at 2 GHz
+constexpr uint32_t kSleepHintNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort = 1;
