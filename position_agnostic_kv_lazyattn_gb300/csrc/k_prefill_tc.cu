@@ -9,31 +9,34 @@
 //
 // CTA = (request r, KV head h, query pair): two Q tiles of 128 rows, each row a
 // (query token, query head of the group) pair, so every K/V tile and its
-// rotation serve 256 rows of the group. Tiles of 64 keys (4 pages) stream
-// through a 3-stage ring. Roles (16 warps = 4 warpgroups):
-//   warps 0, 2    TMA producers, K ring and V ring: per tile 4 pages x two
+// rotation serve 256 rows of the group. Tiles of 128 keys (8 pages) stream
+// through two-stage K and V rings. Roles (16 warps = 4 warpgroups):
+//   warps 0, 2    TMA producers, K ring and V ring: per tile 8 pages x two
 //                 64-dim boxes (128B swizzle); with K, each page's row
 //                 (cos, sin)(start * theta) of the position table (bulk copy)
-//   warp 1        TMEM owner and single-thread UMMA issuer, per tile:
-//                 S_i = Q_i K^T (fp16, 128x64x128) for both Q tiles, then
-//                 O_i += P_i V of the previous tile (bf16, 128x128x64)
+//                 and the tile's page starts / token counts in a 4-deep ring
+//   warp 1        TMEM owner and single-thread UMMA issuer, per tile k:
+//                 S_0 = Q_0 K^T; O_1 += P_1 V (tile k-1); S_1 = Q_1 K^T;
+//                 O_0 += P_0 V (tile k). QK is fp16 128x128x128 from shared
+//                 memory; PV is bf16 128x128x128 with P read from TMEM.
 //   warps 4-7     softmax of Q tile 0; warps 8-11 softmax of Q tile 1: one row
 //                 per thread (TMEM lane), causal + validity mask on logical
 //                 positions, online softmax in the log2 domain with lazy
-//                 rescaling of O (only when the row max grows by > 8), P as bf16
-//                 to shared memory; final normalisation and store
-//   warps 12-15   K rotation: half a key row per thread; cos/sin of start+slot by
-//                 angle addition of the page's row and a 16-row slot table kept
-//                 in shared memory; written back in place as fp16
-// S is double-buffered per Q tile in TMEM (4 x 64 columns) next to O (2 x 128).
+//                 rescaling of O (only when the row max grows by > 8); P is
+//                 written as bf16 over the first 64 columns of its own S
+//   warps 12-15   K rotation: thread = (slot, 8 frequencies), so the slot's
+//                 (cos, sin)(slot * theta) stay in registers; per page the
+//                 start's row from shared memory; cos/sin(start + slot) by angle
+//                 addition; written back in place as fp16
+// TMEM: S_0, S_1, O_0, O_1, 128 columns each. P_i aliases S_i: the MMA that
+// next overwrites S_i is issued after the PV MMA that reads P_i, and
+// tcgen05.mma operations of one thread execute in issue order. The same order
+// means that when softmax i sees S_i of tile k, O_i already holds tile k-1.
 // Tiles whose keys are all masked for every row of the CTA (past the causal
 // edge, or empty entries) are skipped. Only the producer reads the block
-// table: with each stage it publishes the tile's page starts and token counts
-// in shared memory (before arriving on the stage's barrier), and after the last
-// tile a sentinel stage, so the consumer roles never touch global memory inside
-// the tile loop. Every wait is
-// bounded; a timeout raises an abort flag that all roles honour, drains
-// in-flight copies and MMAs, frees TMEM and records LAZYATTN_EDEVICE.
+// table. Every wait is bounded; a timeout raises an abort flag that all roles
+// honour, drains in-flight copies and MMAs, frees TMEM and records
+// LAZYATTN_EDEVICE.
 #include <limits.h>
 
 #include "internal.h"
@@ -49,33 +52,30 @@ constexpr int kD = 128;
 constexpr int kTileM = 128;                        // rows per Q tile (one TMEM lane each)
 constexpr int kQTiles = 2;
 constexpr int kRows = kTileM * kQTiles;
-constexpr int kN = 64;                             // keys per K/V tile
-constexpr int kPagesPerTile = kN / kPage;          // 4
-constexpr int kStages = 3;
+constexpr int kN = 128;                            // keys per K/V tile
+constexpr int kPagesPerTile = kN / kPage;          // 8
+constexpr int kStages = 2;
+constexpr int kInfoSlots = 4;                      // tile-info ring (power of two)
 constexpr int kThreads = 512;
 constexpr int kQBytes = kTileM * kD * 2;           // 32 KB
 constexpr int kQChunk = kTileM * 128;              // 16 KB (64 dims)
-constexpr int kKVBytes = kN * kD * 2;              // 16 KB
-constexpr int kKVChunk = kN * 128;                 // 8 KB (64 dims)
-constexpr int kBaseBytes = kPagesPerTile * 512;    // 4 position-table rows
-constexpr int kPBytes = kTileM * kN * 2;           // 16 KB
-constexpr int kSlotRow = 528;                      // 512 B + 16 B pad (conflict-free column reads)
+constexpr int kKVBytes = kN * kD * 2;              // 32 KB
+constexpr int kKVChunk = kN * 128;                 // 16 KB (64 dims)
+constexpr int kBaseBytes = kPagesPerTile * 512;    // 8 position-table rows
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQTiles * kQBytes;
 constexpr int kOffV = kOffK + kStages * kKVBytes;
-constexpr int kOffP = kOffV + kStages * kKVBytes;
-constexpr int kOffBase = kOffP + kQTiles * kPBytes;
-constexpr int kOffSlot = kOffBase + kStages * kBaseBytes;
-constexpr int kSmemUsed = kOffSlot + kPage * kSlotRow;
+constexpr int kOffBase = kOffV + kStages * kKVBytes;
+constexpr int kSmemUsed = kOffBase + kStages * kBaseBytes;
 constexpr int kSmemBytes = kSmemUsed + 1024;       // + alignment slack
-constexpr uint32_t kTmemCols = 512;                // S[i][b] at i*128 + b*64; O[i] at 256 + i*128
+constexpr uint32_t kTmemCols = 512;                // S_i at i*128 (P_i in its first 64), O_i at 256 + i*128
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzled tiles need 1 KB alignment");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// What the producer tells the consumers about the tile in a stage.
+// What the producer tells the consumers about a tile.
 struct TileInfo {
     int j;                        // tile index, -1: no more tiles
     int start[kPagesPerTile];     // logical position of slot 0 of each page
@@ -117,6 +117,32 @@ __device__ __forceinline__ uint4 pack8_h(const float (&x)[8]) {
     return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
 }
 
+// max of three (one instruction on this architecture)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Two fp32 lanes per instruction (packed f32x2 arithmetic).
+__device__ __forceinline__ float2 sub2(float2 a, float m) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %3};\n\t"
+        "sub.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(m));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "add.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
 // Entry check shared by every role so that all of them agree on which slots
 // hold keys: page in range and positions inside the table.
 __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
@@ -150,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     __shared__ uint64_t bar_kfull[kStages], bar_kempty[kStages], bar_vfull[kStages], bar_vempty[kStages];
-    __shared__ uint64_t bar_kready[kStages];
-    __shared__ uint64_t bar_sfull[kQTiles][2], bar_sfree[kQTiles][2], bar_pfull[kQTiles], bar_odone[kQTiles];
+    __shared__ uint64_t bar_kready[kStages], bar_info[kInfoSlots];
+    __shared__ uint64_t bar_sfull[kQTiles], bar_pfull[kQTiles], bar_odone[kQTiles];
     __shared__ uint64_t bar_qready, bar_drain;
-    __shared__ TileInfo s_info[kStages];
+    __shared__ TileInfo s_info[kInfoSlots];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -185,11 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bar_vempty[s]), 1);
             mbar_init(smem_u32(&bar_kready[s]), 128);
         }
+        for (int s = 0; s < kInfoSlots; ++s) mbar_init(smem_u32(&bar_info[s]), 1);
         for (int i = 0; i < kQTiles; ++i) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(smem_u32(&bar_sfull[i][b]), 1);
-                mbar_init(smem_u32(&bar_sfree[i][b]), 128);
-            }
+            mbar_init(smem_u32(&bar_sfull[i]), 1);
             mbar_init(smem_u32(&bar_pfull[i]), 128);
             mbar_init(smem_u32(&bar_odone[i]), 1);
         }
@@ -212,7 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Warp 0 streams K tiles (with the pages' position-table rows and the
         // tile info), warp 2 streams V tiles, each through its own ring: a K
         // stage is reused once the tile's QK MMAs are done, a V stage once its PV
-        // MMAs are, so both loads are requested several tiles ahead.
+        // MMAs are. The info ring needs no wait of its own: slot k % 4 last held
+        // tile k - 4, and the K stage wait for tile k (QK of tile k - 2 done)
+        // already implies that the PV MMAs of tile k - 3, and so every reader of
+        // tile k - 4's info, are done.
         const bool is_k = warp == 0;
         if (lane == 0 && T > 0) {
             uint64_t* full = is_k ? bar_kfull : bar_vfull;
@@ -233,9 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t fb = smem_u32(&full[st]);
-                TileInfo& info = s_info[st];
+                TileInfo& info = s_info[k & (kInfoSlots - 1)];
+                const uint32_t ib = smem_u32(&bar_info[k & (kInfoSlots - 1)]);
                 if (j == T) {   // sentinel: no more tiles
                     info.j = -1;
+                    mbar_arrive(ib);
                     mbar_arrive(fb);
                     break;
                 }
@@ -243,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
                 int ys[kPagesPerTile];
                 const float2* bases[kPagesPerTile];
+#pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     const int idx = e0 + j * kPagesPerTile + p;
                     int y = P.oob_row, n = 0, st0 = 0;
@@ -264,9 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ys[p] = y;
                     bases[p] = base;
                 }
-                if (is_k) info.j = j;
-                // arrive before the copies: releases the info writes to the waiters
+                if (is_k) {
+                    info.j = j;
+                    mbar_arrive(ib);   // releases the info writes to the softmax roles
+                }
+                // arrive before the copies: releases the info writes to the K waiters
                 mbar_arrive_expect_tx(fb, is_k ? kKVBytes + kBaseBytes : kKVBytes);
+#pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     tma_load_2d(ds + p * 2048, map, 0, ys[p], fb);
                     tma_load_2d(ds + kKVChunk + p * 2048, map, 64, ys[p], fb);
@@ -290,71 +324,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = tile1 ? 2 : 1;
             // Descriptors are built once; a k-step only moves the start address,
             // i.e. adds (byte offset >> 4) to the low field of the descriptor.
-            // Q tiles, P tiles and ring stages are evenly spaced: index * stride.
+            // Q tiles and ring stages are evenly spaced: index * stride.
             const uint64_t dq0 = sdesc_sw128(smem_u32(sm + kOffQ), 16, 1024);
-            const uint64_t dp0 = sdesc_sw128(smem_u32(sm + kOffP), 16, 1024);
             const uint64_t dk0 = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
             const uint64_t dv0 = sdesc_sw128(smem_u32(sm + kOffV), kKVChunk, 1024);
-            auto issue_qk = [&](int i, int st, int b) {
+            auto issue_qk = [&](int i, int st) {
                 const uint64_t a0 = dq0 + (uint64_t)(i * (kQBytes >> 4)), b0 = dk0 + (uint64_t)(st * (kKVBytes >> 4));
-                const uint32_t d = tmem + i * 128 + b * kN;
+                const uint32_t d = tmem + i * 128;
 #pragma unroll
                 for (int t = 0; t < kD / 16; ++t) {
                     const uint64_t oa = (uint64_t)(((t >> 2) * kQChunk + (t & 3) * 32) >> 4);
                     const uint64_t ob = (uint64_t)(((t >> 2) * kKVChunk + (t & 3) * 32) >> 4);
                     umma_f16(d, a0 + oa, b0 + ob, idqk, t > 0 ? 1u : 0u);
                 }
+                umma_commit(smem_u32(&bar_sfull[i]));
             };
-            auto issue_pv = [&](int i, int st, uint32_t first) {
-                const uint64_t a0 = dp0 + (uint64_t)(i * (kPBytes >> 4)), b0 = dv0 + (uint64_t)(st * (kKVBytes >> 4));
-                const uint32_t d = tmem + 256 + i * 128;
+            // O_i += P_i V: P_i (bf16, 128 x 128 keys) is the first 64 columns of S_i.
+            auto issue_pv = [&](int i, int st, bool first) {
+                const uint64_t b0 = dv0 + (uint64_t)(st * (kKVBytes >> 4));
+                const uint32_t d = tmem + 256 + i * 128, a = tmem + i * 128;
 #pragma unroll
                 for (int t = 0; t < kN / 16; ++t)
-                    umma_f16(d, a0 + (uint64_t)(t * 2), b0 + (uint64_t)(t * 128), idpv, (t > 0 || !first) ? 1u : 0u);
+                    umma_f16_ts(d, a + 8 * t, b0 + (uint64_t)(t * 128), idpv, (t > 0 || !first) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_odone[i]));
             };
             bool ok = T > 0 && mbar_wait(smem_u32(&bar_qready), 0, abort_flag);
             int k = 0;
             for (; ok;) {
-                const int st = k % kStages, b = k & 1;
-                ok = mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag);
-                if (!ok || s_info[st].j < 0) break;
-                ok = mbar_wait(smem_u32(&bar_kready[st]), (k / kStages) & 1, abort_flag);
+                const int st = k % kStages, ph = (k / kStages) & 1;
+                ok = mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag);
+                if (!ok || s_info[k & (kInfoSlots - 1)].j < 0) break;
+                ok = mbar_wait(smem_u32(&bar_kready[st]), ph, abort_flag);
                 if (!ok) break;
-                for (int i = 0; ok && i < nt; ++i) {
-                    if (k >= 2) ok = mbar_wait(smem_u32(&bar_sfree[i][b]), ((k >> 1) - 1) & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(i, st, b);
-                    umma_commit(smem_u32(&bar_sfull[i][b]));
-                }
-                if (!ok) break;
-                umma_commit(smem_u32(&bar_kempty[st]));   // K stage free once these QK MMAs finish
-                if (k >= 1) {   // P V of the previous tile
-                    const int pst = (k - 1) % kStages;
-                    ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
-                    for (int i = 0; ok && i < nt; ++i) {
-                        ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
+                tc_fence_after();
+                issue_qk(0, st);
+                if (nt == 2) {
+                    if (k >= 1) {   // P_1 V of the previous tile, then S_1 may be overwritten
+                        ok = mbar_wait(smem_u32(&bar_pfull[1]), (k - 1) & 1, abort_flag);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(i, pst, k == 1);
-                        umma_commit(smem_u32(&bar_odone[i]));
+                        const int pst = (k - 1) % kStages;
+                        issue_pv(1, pst, k == 1);
+                        umma_commit(smem_u32(&bar_vempty[pst]));
                     }
-                    if (!ok) break;
-                    umma_commit(smem_u32(&bar_vempty[pst]));
+                    issue_qk(1, st);
                 }
+                umma_commit(smem_u32(&bar_kempty[st]));   // K stage free once these QK MMAs finish
+                ok = mbar_wait(smem_u32(&bar_vfull[st]), ph, abort_flag) &&
+                     mbar_wait(smem_u32(&bar_pfull[0]), k & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, st, k == 0);
+                if (nt == 1) umma_commit(smem_u32(&bar_vempty[st]));
                 ++k;
             }
-            if (ok && k >= 1) {   // P V of the last tile
-                const int pst = (k - 1) % kStages;
-                ok = mbar_wait(smem_u32(&bar_vfull[pst]), ((k - 1) / kStages) & 1, abort_flag);
-                for (int i = 0; ok && i < nt; ++i) {
-                    ok = mbar_wait(smem_u32(&bar_pfull[i]), (k - 1) & 1, abort_flag);
-                    if (!ok) break;
+            if (ok && nt == 2 && k >= 1) {   // P_1 V of the last tile
+                ok = mbar_wait(smem_u32(&bar_pfull[1]), (k - 1) & 1, abort_flag);
+                if (ok) {
                     tc_fence_after();
-                    issue_pv(i, pst, k == 1);
-                    umma_commit(smem_u32(&bar_odone[i]));
+                    const int pst = (k - 1) % kStages;
+                    issue_pv(1, pst, k == 1);
+                    umma_commit(smem_u32(&bar_vempty[pst]));
                 }
-                umma_commit(smem_u32(&bar_vempty[pst]));
             }
             // every issued MMA has finished before TMEM / smem are released
             umma_commit(smem_u32(&bar_drain));
@@ -363,74 +394,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ K rotation
+        // Thread = (slot, group u of 8 frequencies): dims 8u..8u+7 of the first
+        // half and 64+8u.. of the second half of every key row with this slot.
         const int rt = threadIdx.x - 384;
-        uint8_t* slot_tab = sm + kOffSlot;   // row t: (cos, sin)(t * theta_i)
-        for (int i = rt; i < kPage * 32; i += 128) {
-            const int t = i >> 5, f4 = i & 31;
-            const float4 v = t < pv.max_position ? __ldg(reinterpret_cast<const float4*>(pv.rope) + t * 32 + f4)
-                                                 : make_float4(1.f, 0.f, 1.f, 0.f);
-            *reinterpret_cast<float4*>(slot_tab + t * kSlotRow + f4 * 16) = v;
+        const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
+        float cs[8], sn[8];   // (cos, sin)(slot * theta_f), f = 8u + 0..7
+        {
+            const float4* t4 = reinterpret_cast<const float4*>(pv.rope + (size_t)slot * (kD / 2) + 8 * u);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
+                cs[2 * v] = f.x;
+                sn[2 * v] = f.y;
+                cs[2 * v + 1] = f.z;
+                sn[2 * v + 1] = f.w;
+            }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");   // slot table complete (rotation warps only)
-        const int kr = rt >> 1, hf = rt & 1;              // key row of the tile, half of its units
-        const int slot = kr & 15;
         for (int k = 0; T > 0; ++k) {
-            const int st = k % kStages;
-            if (!mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag)) break;
-            const TileInfo& info = s_info[st];
+            const int st = k % kStages, ph = (k / kStages) & 1;
+            if (!mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag)) break;
+            const TileInfo& info = s_info[k & (kInfoSlots - 1)];
             if (info.j < 0) break;
-            const bool valid = slot < info.n[kr >> 4];
+            int n[kPagesPerTile];
             bool partial = false;   // a page with some, but not all, slots holding keys
 #pragma unroll
-            for (int p = 0; p < kPagesPerTile; ++p) partial = partial || (info.n[p] > 0 && info.n[p] < kPage);
+            for (int p = 0; p < kPagesPerTile; ++p) {
+                n[p] = info.n[p];
+                partial = partial || (n[p] > 0 && n[p] < kPage);
+            }
             uint8_t* kb = sm + kOffK + st * kKVBytes;
             uint8_t* vb = sm + kOffV + st * kKVBytes;
-            if (valid) {
-                const float4* base = reinterpret_cast<const float4*>(sm + kOffBase + st * kBaseBytes + (kr >> 4) * 512);
-                const float4* sl = reinterpret_cast<const float4*>(slot_tab + slot * kSlotRow);
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const int u = 4 * hf + uu;
-                    uint4* p1 = reinterpret_cast<uint4*>(kb + sw128_offset(kr, u));
-                    uint4* p2 = reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u));
+            const uint8_t* bb = sm + kOffBase + st * kBaseBytes + u * 64;
+#pragma unroll 2
+            for (int p = 0; p < kPagesPerTile; ++p) {
+                const int kr = p * kPage + slot;
+                uint4* p1 = reinterpret_cast<uint4*>(kb + sw128_offset(kr, u));
+                uint4* p2 = reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u));
+                if (slot < n[p]) {
                     float x1[8], x2[8];
                     unpack8(*p1, x1);
                     unpack8(*p2, x2);
                     if (!PREROT) {
+                        const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1
-                            const float4 b4 = base[4 * u + v], s4 = sl[4 * u + v];
-                            const float c0 = b4.x * s4.x - b4.y * s4.y, n0 = b4.y * s4.x + b4.x * s4.y;
-                            const float c1 = b4.z * s4.z - b4.w * s4.w, n1 = b4.w * s4.z + b4.z * s4.w;
-                            const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
-                            x1[2 * v] = a0 * c0 - z0 * n0;
-                            x2[2 * v] = a0 * n0 + z0 * c0;
-                            x1[2 * v + 1] = a1 * c1 - z1 * n1;
-                            x2[2 * v + 1] = a1 * n1 + z1 * c1;
+                            const float4 b = b4[v];
+#pragma unroll
+                            for (int w = 0; w < 2; ++w) {
+                                const int f = 2 * v + w;
+                                const float cb = w ? b.z : b.x, sb = w ? b.w : b.y;
+                                const float c = cb * cs[f] - sb * sn[f], s = sb * cs[f] + cb * sn[f];
+                                const float a = x1[f], z = x2[f];
+                                x1[f] = a * c - z * s;
+                                x2[f] = a * s + z * c;
+                            }
                         }
                     }
                     *p1 = pack8_h(x1);
                     *p2 = pack8_h(x2);
-                }
-            } else {   // no key in this slot: zero K so that its scores stay finite
-                const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const int u = 4 * hf + uu;
-                    *reinterpret_cast<uint4*>(kb + sw128_offset(kr, u)) = z;
-                    *reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u)) = z;
+                } else {   // no key in this slot: zero K so that its scores stay finite
+                    *p1 = make_uint4(0, 0, 0, 0);
+                    *p2 = make_uint4(0, 0, 0, 0);
                 }
             }
             if (partial) {   // stale slots of a partly filled page: zero V too (0 * NaN would be NaN)
-                if (!mbar_wait(smem_u32(&bar_vfull[st]), (k / kStages) & 1, abort_flag)) break;
-                if (!valid) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        const int u = 4 * hf + uu;
-                        *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = z;
-                        *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = z;
-                    }
+                if (!mbar_wait(smem_u32(&bar_vfull[st]), ph, abort_flag)) break;
+#pragma unroll 1
+                for (int p = 0; p < kPagesPerTile; ++p) {
+                    if (slot < n[p]) continue;
+                    const int kr = p * kPage + slot;
+                    *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
@@ -443,6 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int trow = 32 * quarter + lane;      // row within the tile = TMEM lane
         const int row = qi * kTileM + trow;        // row within the CTA
         const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
+        const uint32_t ts = tl + qi * 128;         // S_i, and P_i over its first 64 columns
+        const uint32_t to = tl + 256 + qi * 128;   // O_i
         const int t_local = row / g, jh = row - t_local * g;
         const int tok = i0 + t_local;
         const int m_row = qs + tok;
@@ -490,86 +526,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int k = 0;
         for (; active && T > 0; ++k) {
-            const int st = k % kStages, b = k & 1;
-            ok = mbar_wait(smem_u32(&bar_kfull[st]), (k / kStages) & 1, abort_flag);
+            const int is = k & (kInfoSlots - 1);
+            ok = mbar_wait(smem_u32(&bar_info[is]), (k / kInfoSlots) & 1, abort_flag);
             if (!ok) break;
-            const TileInfo& info = s_info[st];
+            const TileInfo& info = s_info[is];
             if (info.j < 0) break;
-            // which keys of the tile this row may see
-            int kstart[kPagesPerTile], kn[kPagesPerTile];
-            bool full = row_valid;
+            // keys of page p visible to this row: slots [0, lim[p])
+            int lim[kPagesPerTile];
+            bool full = true;
 #pragma unroll
             for (int p = 0; p < kPagesPerTile; ++p) {
-                kstart[p] = info.start[p];
-                kn[p] = info.n[p];
-                full = full && (kn[p] == kPage) && (kstart[p] + kPage - 1 <= m_row);
+                const int l = min(info.n[p], m_row - info.start[p] + 1);
+                lim[p] = row_valid ? max(l, 0) : 0;
+                full = full && lim[p] == kPage;
             }
-            ok = mbar_wait(smem_u32(&bar_sfull[qi][b]), (k >> 1) & 1, abort_flag);
+            // a warp whose rows all see every key of the tile skips the masking
+            const bool wfull = __all_sync(0xffffffffu, full);
+            ok = mbar_wait(smem_u32(&bar_sfull[qi]), k & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            float s[kN];
+            // pass 1: row maximum over the tile (masked keys are -inf)
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < kN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + qi * 128 + b * kN + 32 * c, v);
+            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(v[i]);
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_sfree[qi][b]));
-            if (!full) {
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[64];
+                tmem_ld64(ts + 64 * hh, v);
+                if (wfull) {
 #pragma unroll
-                for (int kk = 0; kk < kN; ++kk) {
-                    const int p = kk >> 4, sl = kk & 15;
-                    const bool vis = row_valid && sl < kn[p] && kstart[p] + sl <= m_row;
-                    s[kk] = vis ? s[kk] : -INFINITY;
+                    for (int j = 0; j < 32; ++j)
+                        mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int key = 64 * hh + 2 * j, l = lim[key >> 4];
+                        const float s0 = (key & 15) < l ? __uint_as_float(v[2 * j]) : -INFINITY;
+                        const float s1 = ((key + 1) & 15) < l ? __uint_as_float(v[2 * j + 1]) : -INFINITY;
+                        mx8[j & 7] = fmax3(mx8[j & 7], s0, s1);
+                    }
                 }
             }
-            float mx8[8];   // eight independent chains instead of one 64-long one
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) mx8[kk] = s[kk];
-#pragma unroll
-            for (int kk = 8; kk < kN; ++kk) mx8[kk & 7] = fmaxf(mx8[kk & 7], s[kk]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             float alpha = 1.f;
             if (mx > m_run + kRescaleThreshold) {
                 alpha = fast_exp2(m_run - mx);   // 0 when m_run is -inf
                 m_run = mx;
             }
             const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[kN / 2];
-#pragma unroll
-            for (int kk = 0; kk < kN; kk += 2) {
-                const float p0 = fast_exp2(s[kk] - mref), p1 = fast_exp2(s[kk + 1] - mref);
-                sum8[(kk >> 1) & 7] += p0 + p1;
-                pk[kk / 2] = pack_bf2(p0, p1);
-            }
-            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-            l_run = l_run * alpha + sum;
-            if (k >= 1) {
-                ok = mbar_wait(smem_u32(&bar_odone[qi]), (k - 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // O_i already holds tiles < k (see the header); rescale it when the
+            // reference maximum moved for some row of the warp.
+            if (k >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(tl + 256 + qi * 128 + 32 * c, v);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(to + 32 * c, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        tmem_st32(tl + 256 + qi * 128 + 32 * c, v);
-                    }
-                    tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st32(to + 32 * c, v);
                 }
             }
-            uint8_t* ps = sm + kOffP + qi * kPBytes;
+            // pass 2: P = 2^(s - mref) as bf16 pairs over S's first 64 columns
+            float2 sum4[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4*>(ps + sw128_offset(trow, u)) =
-                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-            fence_proxy_async_smem();
+            for (int i = 0; i < 4; ++i) sum4[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[64];
+                tmem_ld64(ts + 64 * hh, v);
+                uint32_t pk[32];
+                if (wfull) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 d = sub2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref);
+                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        sum4[j & 3] = add2(sum4[j & 3], pp);
+                        pk[j] = pack_bf2(pp.x, pp.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int key = 64 * hh + 2 * j, l = lim[key >> 4];
+                        const float s0 = (key & 15) < l ? __uint_as_float(v[2 * j]) : -INFINITY;
+                        const float s1 = ((key + 1) & 15) < l ? __uint_as_float(v[2 * j + 1]) : -INFINITY;
+                        const float2 d = sub2(make_float2(s0, s1), mref);
+                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        sum4[j & 3] = add2(sum4[j & 3], pp);
+                        pk[j] = pack_bf2(pp.x, pp.y);
+                    }
+                }
+                tmem_st32(ts + 32 * hh, pk);
+            }
+            const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]);
+            const float2 s4 = add2(s01, s23);
+            l_run = l_run * alpha + (s4.x + s4.y);
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_pfull[qi]));
         }
@@ -584,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
                 if (k >= 1 && ok) {
-                    tmem_ld32(tl + 256 + qi * 128 + 32 * c, v);
+                    tmem_ld32(to + 32 * c, v);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0u;
