@@ -80,6 +80,7 @@ struct TileInfo {
     int j;                        // tile index, -1: no more tiles
     int start[kPagesPerTile];     // logical position of slot 0 of each page
     int n[kPagesPerTile];         // keys in each page (0: none / unusable)
+    int y[kPagesPerTile];         // row of the page in the K/V tensor maps (out of range: zero fill)
 };
 
 struct PrefillParams {
@@ -152,22 +153,6 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
     return n;
 }
 
-// A tile is processed iff one of its pages holds a key at a position <= the
-// largest query position of the CTA. Every role evaluates this identically.
-__device__ __forceinline__ bool tile_live(const PoolView& pv, const uint64_t* entries, int e0, int e1, int j,
-                                          int m_hi) {
-    bool live = false;
-#pragma unroll
-    for (int p = 0; p < kPagesPerTile; ++p) {
-        const int idx = e0 + j * kPagesPerTile + p;
-        if (idx < e1) {
-            const uint64_t e = entries[idx];
-            live = live || (usable_tokens(pv, e) > 0 && entry_start(e) <= m_hi);
-        }
-    }
-    return live;
-}
-
 template <bool PREROT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, PoolView pv,
@@ -231,89 +216,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
 
-    if (warp == 0 || warp == 2) {
-        // ------------------------------------------------------------ TMA producers
-        // Warp 0 streams K tiles (with the pages' position-table rows and the
-        // tile info), warp 2 streams V tiles, each through its own ring: a K
-        // stage is reused once the tile's QK MMAs are done, a V stage once its PV
-        // MMAs are. The info ring needs no wait of its own: slot k % 4 last held
-        // tile k - 4, and the K stage wait for tile k (QK of tile k - 2 done)
-        // already implies that the PV MMAs of tile k - 3, and so every reader of
-        // tile k - 4's info, are done.
-        const bool is_k = warp == 0;
+    if (warp == 0) {
+        // ------------------------------------------------------------ K producer
+        // Reads the block table (entries of tile j + 1 are loaded while tile j is
+        // issued), decides which tiles are live, publishes each live tile's info
+        // (page starts, token counts, tensor-map rows) in a 4-deep ring, and
+        // streams K tiles with their pages' position-table rows. A K stage is
+        // reused once the tile's QK MMAs are done. The info ring needs no wait
+        // of its own: slot k % 4 last held tile k - 4, and the K stage wait for
+        // tile k (QK of tile k - 2 done) already implies that the PV MMAs of
+        // tile k - 3, and so every reader of tile k - 4's info, are done.
+        // A tile is live iff one of its pages holds a key at a position <= the
+        // largest query position of the CTA.
         if (lane == 0 && T > 0) {
-            uint64_t* full = is_k ? bar_kfull : bar_vfull;
-            uint64_t* empty = is_k ? bar_kempty : bar_vempty;
-            const CUtensorMap* map = is_k ? &kmap : &vmap;
-            const int off = is_k ? kOffK : kOffV;
+            auto load_entries = [&](int jj, uint64_t (&e)[kPagesPerTile]) {
+#pragma unroll
+                for (int p = 0; p < kPagesPerTile; ++p) {
+                    const int idx = e0 + jj * kPagesPerTile + p;
+                    const uint64_t v = P.entries[min(idx, e1 - 1)];
+                    e[p] = idx < e1 ? v : 0ull;   // 0: an empty entry
+                }
+            };
             int last_k[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s) last_k[s] = -1;
+            uint64_t cur[kPagesPerTile], nxt[kPagesPerTile] = {};
+            load_entries(0, cur);
             int k = 0;
             bool ok = true;
             for (int j = 0; j <= T; ++j) {
-                if (j < T && !tile_live(pv, P.entries, e0, e1, j, m_hi)) continue;
-                if (j == T && !is_k) break;
-                const int st = k % kStages;
-                if (k >= kStages && !mbar_wait(smem_u32(&empty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = smem_u32(&full[st]);
-                TileInfo& info = s_info[k & (kInfoSlots - 1)];
-                const uint32_t ib = smem_u32(&bar_info[k & (kInfoSlots - 1)]);
-                if (j == T) {   // sentinel: no more tiles
-                    info.j = -1;
-                    mbar_arrive(ib);
-                    mbar_arrive(fb);
-                    break;
-                }
-                const uint32_t ds = smem_u32(sm + off + st * kKVBytes);
-                const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
-                int ys[kPagesPerTile];
-                const float2* bases[kPagesPerTile];
+                if (j + 1 < T) load_entries(j + 1, nxt);
+                int n[kPagesPerTile];
+                bool live = false;
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
-                    const int idx = e0 + j * kPagesPerTile + p;
-                    int y = P.oob_row, n = 0, st0 = 0;
-                    const float2* base = pv.rope;
-                    if (idx < e1) {
-                        const uint64_t e = P.entries[idx];
-                        n = usable_tokens(pv, e);
-                        st0 = entry_start(e);
-                        if (n < 0 && is_k) record_error(pv.status, LAZYATTN_ERANGE);
-                        if (n > 0) {
-                            y = ((int)entry_page(e) * Hkv + h) * kPage;
-                            base = pv.rope + (size_t)st0 * (kD / 2);
-                        }
-                    }
-                    if (is_k) {
-                        info.start[p] = st0;
-                        info.n[p] = max(n, 0);
-                    }
-                    ys[p] = y;
-                    bases[p] = base;
+                    n[p] = j < T ? usable_tokens(pv, cur[p]) : 0;
+                    live = live || (n[p] > 0 && entry_start(cur[p]) <= m_hi);
                 }
-                if (is_k) {
+                if (j == T || live) {
+                    const int st = k % kStages;
+                    if (k >= kStages && !mbar_wait(smem_u32(&bar_kempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bar_kfull[st]);
+                    TileInfo& info = s_info[k & (kInfoSlots - 1)];
+                    const uint32_t ib = smem_u32(&bar_info[k & (kInfoSlots - 1)]);
+                    if (j == T) {   // sentinel: no more tiles
+                        info.j = -1;
+                        mbar_arrive(ib);
+                        mbar_arrive(fb);
+                        break;
+                    }
+                    const uint32_t ds = smem_u32(sm + kOffK + st * kKVBytes);
+                    const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
+                    int ys[kPagesPerTile];
+#pragma unroll
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        if (n[p] < 0) record_error(pv.status, LAZYATTN_ERANGE);
+                        ys[p] = n[p] > 0 ? ((int)entry_page(cur[p]) * Hkv + h) * kPage : P.oob_row;
+                        info.start[p] = entry_start(cur[p]);
+                        info.n[p] = max(n[p], 0);
+                        info.y[p] = ys[p];
+                    }
                     info.j = j;
-                    mbar_arrive(ib);   // releases the info writes to the softmax roles
-                }
-                // arrive before the copies: releases the info writes to the K waiters
-                mbar_arrive_expect_tx(fb, is_k ? kKVBytes + kBaseBytes : kKVBytes);
+                    mbar_arrive(ib);   // releases the info writes to the other roles
+                    mbar_arrive_expect_tx(fb, kKVBytes + kBaseBytes);
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    tma_load_2d(ds + p * 2048, map, 0, ys[p], fb);
-                    tma_load_2d(ds + kKVChunk + p * 2048, map, 64, ys[p], fb);
-                    if (is_k) bulk_load(bs + p * 512, bases[p], 512, fb);
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
+                        tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
+                        const float2* base = pv.rope + (n[p] > 0 ? (size_t)entry_start(cur[p]) * (kD / 2) : 0);
+                        bulk_load(bs + p * 512, base, 512, fb);
+                    }
+                    last_k[st] = k;
+                    ++k;
                 }
-                last_k[st] = k;
-                ++k;
+#pragma unroll
+                for (int p = 0; p < kPagesPerTile; ++p) cur[p] = nxt[p];
             }
             if (!ok) *abort_flag = 1;
             if (*abort_flag) {   // let issued copies land before the CTA's smem is released
                 volatile int never = 0;
                 for (int s = 0; s < kStages; ++s)
-                    if (last_k[s] >= 0) mbar_wait(smem_u32(&full[s]), (last_k[s] / kStages) & 1, &never);
+                    if (last_k[s] >= 0) mbar_wait(smem_u32(&bar_kfull[s]), (last_k[s] / kStages) & 1, &never);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ V producer
+        // Takes the page rows from the tile info; a V stage is reused once the
+        // tile's PV MMAs are done.
+        if (lane == 0 && T > 0) {
+            int last_k[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) last_k[s] = -1;
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int st = k % kStages;
+                ok = mbar_wait(smem_u32(&bar_info[k & (kInfoSlots - 1)]), (k / kInfoSlots) & 1, abort_flag);
+                if (!ok) break;
+                const TileInfo& info = s_info[k & (kInfoSlots - 1)];
+                if (info.j < 0) break;
+                int ys[kPagesPerTile];
+#pragma unroll
+                for (int p = 0; p < kPagesPerTile; ++p) ys[p] = info.y[p];
+                if (k >= kStages && !mbar_wait(smem_u32(&bar_vempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bar_vfull[st]);
+                const uint32_t ds = smem_u32(sm + kOffV + st * kKVBytes);
+                mbar_arrive_expect_tx(fb, kKVBytes);
+#pragma unroll
+                for (int p = 0; p < kPagesPerTile; ++p) {
+                    tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
+                    tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                }
+                last_k[st] = k;
+            }
+            if (!ok) *abort_flag = 1;
+            if (*abort_flag) {
+                volatile int never = 0;
+                for (int s = 0; s < kStages; ++s)
+                    if (last_k[s] >= 0) mbar_wait(smem_u32(&bar_vfull[s]), (last_k[s] / kStages) & 1, &never);
             }
         }
     } else if (warp == 1) {
