@@ -556,41 +556,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const TileInfo& info = s_info[is];
             if (info.j < 0) break;
-            // keys of page p visible to this row: slots [0, lim[p])
-            int lim[kPagesPerTile];
-            bool full = true;
+            // visibility of the tile's keys to this row: bit i of visN is key
+            // 32N + i (pages 2N and 2N+1 hold slots [0, lim) of their 16)
+            uint32_t vis[4];
 #pragma unroll
-            for (int p = 0; p < kPagesPerTile; ++p) {
-                const int l = min(info.n[p], m_row - info.start[p] + 1);
-                lim[p] = row_valid ? max(l, 0) : 0;
-                full = full && lim[p] == kPage;
+            for (int w = 0; w < 4; ++w) {
+                uint32_t bits = 0;
+#pragma unroll
+                for (int hp = 0; hp < 2; ++hp) {
+                    const int p = 2 * w + hp;
+                    const int l = row_valid ? max(min(info.n[p], m_row - info.start[p] + 1), 0) : 0;
+                    bits |= ((1u << l) - 1u) << (16 * hp);
+                }
+                vis[w] = bits;
             }
+            const bool full = (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu;
             // a warp whose rows all see every key of the tile skips the masking
             const bool wfull = __all_sync(0xffffffffu, full);
             ok = mbar_wait(smem_u32(&bar_sfull[qi]), k & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            // pass 1: row maximum over the tile (masked keys are -inf)
+            // masked keys read as -inf
+            auto mask64 = [&](uint32_t (&v)[64], int hh) {
+                const uint32_t m0 = hh ? vis[2] : vis[0], m1 = hh ? vis[3] : vis[1];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const uint32_t m = i < 32 ? m0 : m1;
+                    v[i] = (m >> (i & 31)) & 1u ? v[i] : 0xff800000u;
+                }
+            };
+            // pass 1: row maximum over the tile
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-#pragma unroll
+#pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
-                if (wfull) {
+                if (!wfull) mask64(v, hh);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int key = 64 * hh + 2 * j, l = lim[key >> 4];
-                        const float s0 = (key & 15) < l ? __uint_as_float(v[2 * j]) : -INFINITY;
-                        const float s1 = ((key + 1) & 15) < l ? __uint_as_float(v[2 * j + 1]) : -INFINITY;
-                        mx8[j & 7] = fmax3(mx8[j & 7], s0, s1);
-                    }
-                }
+                for (int j = 0; j < 32; ++j)
+                    mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
             }
             const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             float alpha = 1.f;
@@ -615,30 +621,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             float2 sum4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) sum4[i] = make_float2(0.f, 0.f);
-#pragma unroll
+#pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
+                if (!wfull) mask64(v, hh);
                 uint32_t pk[32];
-                if (wfull) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float2 d = sub2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref);
-                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                        sum4[j & 3] = add2(sum4[j & 3], pp);
-                        pk[j] = pack_bf2(pp.x, pp.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int key = 64 * hh + 2 * j, l = lim[key >> 4];
-                        const float s0 = (key & 15) < l ? __uint_as_float(v[2 * j]) : -INFINITY;
-                        const float s1 = ((key + 1) & 15) < l ? __uint_as_float(v[2 * j + 1]) : -INFINITY;
-                        const float2 d = sub2(make_float2(s0, s1), mref);
-                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                        sum4[j & 3] = add2(sum4[j & 3], pp);
-                        pk[j] = pack_bf2(pp.x, pp.y);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const float2 d = sub2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref);
+                    const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                    sum4[j & 3] = add2(sum4[j & 3], pp);
+                    pk[j] = pack_bf2(pp.x, pp.y);
                 }
                 tmem_st32(ts + 32 * hh, pk);
             }
