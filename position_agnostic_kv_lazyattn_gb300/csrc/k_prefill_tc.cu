@@ -194,15 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bar_kempty[s]), 1);
             mbar_init(smem_u32(&bar_vfull[s]), 1);
             mbar_init(smem_u32(&bar_vempty[s]), 1);
-            mbar_init(smem_u32(&bar_kready[s]), 128);
+            mbar_init(smem_u32(&bar_kready[s]), 4);   // one arrival per rotation warp
         }
         for (int s = 0; s < kInfoSlots; ++s) mbar_init(smem_u32(&bar_info[s]), 1);
         for (int i = 0; i < kQTiles; ++i) {
             mbar_init(smem_u32(&bar_sfull[i]), 1);
-            mbar_init(smem_u32(&bar_pfull[i]), 128);
+            mbar_init(smem_u32(&bar_pfull[i]), 4);   // one arrival per softmax warp
             mbar_init(smem_u32(&bar_odone[i]), 1);
         }
-        mbar_init(smem_u32(&bar_qready), kQTiles * 128);
+        mbar_init(smem_u32(&bar_qready), kQTiles * 4);
         mbar_init(smem_u32(&bar_drain), 1);
         mbar_fence_init();
     }
@@ -377,10 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int k = 0;
             for (; ok;) {
                 const int st = k % kStages, ph = (k / kStages) & 1;
-                ok = mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag);
-                if (!ok || s_info[k & (kInfoSlots - 1)].j < 0) break;
+                // K rotated (the rotation warps arrive for the sentinel too)
                 ok = mbar_wait(smem_u32(&bar_kready[st]), ph, abort_flag);
-                if (!ok) break;
+                if (!ok || s_info[k & (kInfoSlots - 1)].j < 0) break;
                 tc_fence_after();
                 issue_qk(0, st);
                 if (nt == 2) {
@@ -435,11 +434,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sn[2 * v + 1] = f.w;
             }
         }
+        // One thread polls the stage's barrier and a named barrier releases the
+        // other 127: every mbarrier update (each TMA copy's bytes) wakes its
+        // pollers, and 128 pollers would take issue slots from the math roles.
+        auto rot_wait = [&](uint32_t bar, uint32_t parity) {
+            if (rt == 0) mbar_wait(bar, parity, abort_flag);
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            return *abort_flag == 0;
+        };
         for (int k = 0; T > 0; ++k) {
             const int st = k % kStages, ph = (k / kStages) & 1;
-            if (!mbar_wait(smem_u32(&bar_kfull[st]), ph, abort_flag)) break;
+            if (!rot_wait(smem_u32(&bar_kfull[st]), ph)) break;
             const TileInfo& info = s_info[k & (kInfoSlots - 1)];
-            if (info.j < 0) break;
+            if (info.j < 0) {   // no more tiles: let the MMA issuer see the sentinel
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_kready[st]));
+                break;
+            }
             int n[kPagesPerTile];
             bool partial = false;   // a page with some, but not all, slots holding keys
 #pragma unroll
@@ -483,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (partial) {   // stale slots of a partly filled page: zero V too (0 * NaN would be NaN)
-                if (!mbar_wait(smem_u32(&bar_vfull[st]), ph, abort_flag)) break;
+                if (!rot_wait(smem_u32(&bar_vfull[st]), ph)) break;
 #pragma unroll 1
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     if (slot < n[p]) continue;
@@ -493,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_kready[st]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_kready[st]));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax rows
@@ -543,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(qsm + kQChunk + sw128_offset(trow, u)) = w2;
             }
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_qready));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_qready));
         }
         const bool active = qi == 0 || tile1;
 
@@ -641,7 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run = l_run * alpha + (s4.x + s4.y);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_pfull[qi]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_pfull[qi]));
         }
 
         // epilogue: O / l -> bf16 rows of out
