@@ -11,10 +11,12 @@
 // current one; three CTAs (12 warps) share an SM. Per page a warp:
 //   * reads K as MMA A-fragments with ldmatrix (16 tokens x 128 dims),
 //   * rotates every key at position start + slot in registers and rounds it to
-//     fp16; the angle's cos/sin come from angle addition, (start) from the page's
-//     row of the fp32 position table (one 512 B row per page, shared by the
-//     lanes) and (slot) from a 16-row copy of the table kept in shared memory,
-//     so the table adds 1/16 of a page's bytes to the L2 traffic,
+//     fp16; the angle's cos/sin come from angle addition: (start) from the
+//     page's row of the fp32 position table (one 512 B row per page, fetched
+//     one page ahead as one float4 per lane and staged in a per-warp buffer),
+//     (slot) from a 9-row copy of the table in shared memory (slots 8..15 add
+//     the angle of 8 to that of slots 0..7), so the table adds 1/16 of a page's
+//     bytes to the L2 traffic and no global load waits inside the page loop,
 //   * computes S^T = K' Q'^T with m16n8k16 MMAs (N = the group's <= 8 heads),
 //   * runs the online softmax in the log2 domain (q is pre-scaled by
 //     log2(e)/sqrt(D)),
@@ -36,11 +38,13 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 2;
+constexpr int kStages = 2;                        // the entry prefetch below reads exactly kStages pages ahead
 constexpr int kStageBytes = 8192;                 // K tile (2 x 2 KB) + V tile (2 x 2 KB)
-constexpr int kSlotRowBytes = 576;              // 64 (cos, sin) + 64 B pad: conflict-free per-lane reads
+constexpr int kRowBytes = 512;                    // one position-table row: 64 (cos, sin)
+constexpr int kSlotRows = 9;                      // (cos, sin)(t * theta) for t = 0..8
 constexpr int kSlotTableOff = kWarps * kStages * kStageBytes;
-constexpr int kSmemBytes = kSlotTableOff + kPage * kSlotRowBytes + 1024;
+constexpr int kBaseBufOff = kSlotTableOff + kSlotRows * kRowBytes;   // per warp: the current page's row
+constexpr int kSmemBytes = kBaseBufOff + kWarps * kRowBytes + 1024;
 constexpr int kMaxGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -120,6 +124,11 @@ __device__ __forceinline__ void rotate2(uint32_t& x, uint32_t& y, const float4& 
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) { return pack_h2(bf_lo(x), bf_hi(x)); }
 
+// 16-byte unit f4 (frequencies 2*f4, 2*f4+1) of slot-table row t. Odd rows swap
+// the two 64-byte halves, so the lanes of a quarter warp (rows 2q and 2q+1,
+// four consecutive units each) hit eight different bank groups.
+__device__ __forceinline__ int slot_unit(int t, int f4) { return t * (kRowBytes / 16) + (f4 ^ ((t & 1) << 2)); }
+
 template <bool PREROT>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -147,13 +156,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&bar_full[warp][st]), 1);
         mbar_fence_init();
     }
-    uint8_t* slot_tab = sm + kSlotTableOff;   // row t: (cos, sin)(t * theta_i), i < 64
+    float4* slot_tab = reinterpret_cast<float4*>(sm + kSlotTableOff);   // row t: (cos, sin)(t * theta_i)
     if (!PREROT) {
-        for (int i = tid; i < kPage * 32; i += kThreads) {
+        for (int i = tid; i < kSlotRows * 32; i += kThreads) {
             const int t = i >> 5, f4 = i & 31;
             const float4 v = t < pv.max_position ? __ldg(reinterpret_cast<const float4*>(pv.rope) + t * 32 + f4)
                                                  : make_float4(1.f, 0.f, 1.f, 0.f);
-            *reinterpret_cast<float4*>(slot_tab + t * kSlotRowBytes + f4 * 16) = v;
+            slot_tab[slot_unit(t, f4)] = v;
         }
     }
     __syncthreads();
@@ -191,9 +200,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t ring = smem_u32(sm + warp * kStages * kStageBytes);
     volatile int* abort_flag = &s_abort;
 
-    auto issue = [&](int i) {   // lane 0 only
+    auto issue = [&](int i, uint64_t e) {   // lane 0 only; e = entry of page i
         if (i >= n_w) return;
-        const uint64_t e = my_entries[kWarps * i];
         if (usable_tokens(pv, e) <= 0) return;
         const int st = i % kStages;
         const uint32_t bar = smem_u32(&bar_full[warp][st]);
@@ -205,8 +213,22 @@ __global__ void __launch_bounds__(kThreads, 3)
         tma_load_2d(dst + 4096, &vmap, 0, y, bar);
         tma_load_2d(dst + 6144, &vmap, 64, y, bar);
     };
-    if (lane == 0)
-        for (int i = 0; i < kStages; ++i) issue(i);
+    // Entries are read two pages ahead and the page's position-table row one
+    // page ahead (one float4 per lane, staged in the warp's row buffer when
+    // the page comes up), so no global load latency sits inside the page loop.
+    auto entry_at = [&](int i) { return i < n_w ? my_entries[kWarps * i] : 0ull; };
+    auto row_of = [&](uint64_t e) {
+        return (!PREROT && usable_tokens(pv, e) > 0)
+                   ? __ldg(reinterpret_cast<const float4*>(pv.rope + (size_t)entry_start(e) * (kD / 2)) + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4* rowbuf = reinterpret_cast<float4*>(sm + kBaseBufOff + warp * kRowBytes);
+    uint64_t e_cur = entry_at(0), e_n1 = entry_at(1);
+    float4 row_next = row_of(e_cur);
+    if (lane == 0) {
+        issue(0, e_cur);
+        issue(1, e_n1);
+    }
 
     float o[8][4];
 #pragma unroll
@@ -216,23 +238,26 @@ __global__ void __launch_bounds__(kThreads, 3)
     int consumed_upto = -1;
 
     for (int i = 0; i < n_w; ++i) {
-        const uint64_t e = my_entries[kWarps * i];
+        const uint64_t e = e_cur;
+        const uint64_t e_n2 = entry_at(i + 2);
+        const float4 row_cur = row_next;
+        row_next = row_of(e_n1);
         const int nv = usable_tokens(pv, e);
         const int st = i % kStages;
         if (nv < 0 && lane == 0) record_error(pv.status, LAZYATTN_ERANGE);
         if (nv > 0) {
+            if (!PREROT) {
+                rowbuf[lane] = row_cur;
+                __syncwarp();
+            }
             if (!mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, abort_flag)) break;
             phases ^= 1u << st;
             consumed_upto = i;
-            const int start = entry_start(e);
             const uint32_t stg = ring + st * kStageBytes;
 
             // K' = rotated keys as the A operand; k-steps t and t+4 hold the rotate-half
             // partners (dims 16t+.. and 64+16t+..), so they are loaded, rotated and
             // multiplied together: (tokens gr | gr+8) x (dims 16t+2c.. | 16t+2c+8..)
-            const float4* base = reinterpret_cast<const float4*>(pv.rope + (size_t)start * (kD / 2));
-            const float4* sa = reinterpret_cast<const float4*>(slot_tab + gr * kSlotRowBytes);
-            const float4* sb = reinterpret_cast<const float4*>(slot_tab + (gr + 8) * kSlotRowBytes);
             float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -243,13 +268,14 @@ __global__ void __launch_bounds__(kThreads, 3)
                 if (!PREROT) {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        // angle of token t = angle(start) + angle(t); both factors from tables
+                        // angle of token gr = angle(start) + angle(gr), and of token gr + 8
+                        // = that + angle(8); every factor from a table row
                         const int f4 = 8 * t + c + 4 * hf;
-                        const float4 b4 = __ldg(base + f4), x = sa[f4], y = sb[f4];
+                        const float4 b4 = rowbuf[f4], x = slot_tab[slot_unit(gr, f4)], y = slot_tab[slot_unit(8, f4)];
                         const float4 ca = make_float4(b4.x * x.x - b4.y * x.y, b4.y * x.x + b4.x * x.y,
                                                       b4.z * x.z - b4.w * x.w, b4.w * x.z + b4.z * x.w);
-                        const float4 cb = make_float4(b4.x * y.x - b4.y * y.y, b4.y * y.x + b4.x * y.y,
-                                                      b4.z * y.z - b4.w * y.w, b4.w * y.z + b4.z * y.w);
+                        const float4 cb = make_float4(ca.x * y.x - ca.y * y.y, ca.y * y.x + ca.x * y.y,
+                                                      ca.z * y.z - ca.w * y.w, ca.w * y.z + ca.z * y.w);
                         rotate2(lo[2 * hf], hi[2 * hf], ca);
                         rotate2(lo[2 * hf + 1], hi[2 * hf + 1], cb);
                     }
@@ -321,8 +347,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         __syncwarp();
         if (lane == 0) {
             fence_proxy_async_smem();   // this warp's reads of the stage precede the next TMA into it
-            issue(i + kStages);
+            issue(i + kStages, e_n2);
         }
+        e_cur = e_n1;
+        e_n1 = e_n2;
     }
     if (*abort_flag && lane == 0) {
         // drain copies this warp issued but did not consume before the CTA releases its smem
