@@ -464,19 +464,26 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (tid == 0) P.tickets[rh] = 0;
 }
 
+// Splits per (request, KV head). Cost model in units of one page per warp:
+// every wave of CTAs pays a fixed overhead (prologue, pipeline fill, the
+// combine) plus its CTAs' longest page run, so
+//   cost(S) = ceil(CTAs / resident slots) * (kCtaOverhead + pages per warp).
+// Few long-lived CTAs win for small batches; large batches split until the
+// last wave is nearly full.
 int choose_splits(const lazyattn_pool& p, const lazyattn_batch& b) {
+    constexpr double kCtaOverhead = 4.0;
     const long W = (long)b.num_requests * p.d.n_kv_heads;
     const long slots = std::max(p.decode_slots, 1);
+    const long pages = std::max(b.max_entries, 1);
     int best = 1;
-    double best_eff = -1.0;
+    double best_cost = 1e300;
     for (int S = 1; S <= 32; ++S) {
-        if (S > 1 && b.max_entries / S < 8) break;   // keep >= 2 pages per warp
-        const double waves = (double)(W * S) / (double)slots;
-        const double eff = waves / std::ceil(waves);
-        if (waves >= 1.0 && eff >= 0.9) return S;
-        const double score = waves < 1.0 ? waves : eff;
-        if (score > best_eff + 1e-9) {
-            best_eff = score;
+        if (S > 1 && pages / S < 8) break;   // keep >= 2 pages per warp
+        const double waves = std::ceil((double)(W * S) / (double)slots);
+        const double per_warp = std::ceil((double)pages / (double)(S * kWarps));
+        const double cost = waves * (kCtaOverhead + per_warp);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
             best = S;
         }
     }
