@@ -26,6 +26,33 @@ __host__ __device__ __forceinline__ uint64_t make_entry(uint32_t page, int32_t s
            ((uint64_t)(w ? 1 : 0) << 63);
 }
 
+// ---------------------------------------------------------------- dependent launches
+// Programmatic dependent launch: a kernel launched with launch_dependent may
+// start while the previous kernel in the stream still runs. It must call
+// grid_dep_wait() before reading anything that kernel writes; the wait
+// returns once the previous grid has completed and its writes are visible
+// (and at once when there is no such dependency). grid_dep_launch_dependents()
+// lets the next such launch start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Shape and buffers a kernel needs about the pool (passed by value).
 struct PoolView {
     void* k_pool;

@@ -144,13 +144,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int gr = lane >> 2, c = lane & 3;
     const int g = P.g, Hq = pv.hq, Hkv = pv.hkv, S = P.splits;
 
-    const int m = P.qpos[r];
-    __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
-    if (m < 0) {   // request without an appended token (status already recorded)
-        if (s == 0)
-            for (int i = tid; i < g * kD; i += kThreads) out_rh[i] = __float2bfloat16_rn(0.f);
-        return;
-    }
+    // Launched as a programmatic dependent of the append kernel: the set-up
+    // below touches nothing the append writes; grid_dep_wait() comes before
+    // the appended position, the table and the pool are read.
+    grid_dep_launch_dependents();
     if (tid == 0) s_abort = 0;
     if (lane == 0) {
         for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&bar_full[warp][st]), 1);
@@ -166,6 +163,14 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
     }
     __syncthreads();
+    grid_dep_wait();
+    const int m = P.qpos[r];
+    __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
+    if (m < 0) {   // request without an appended token (status already recorded)
+        if (s == 0)
+            for (int i = tid; i < g * kD; i += kThreads) out_rh[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
 
     // q of head gr, rotated at m and pre-scaled, as the B operand of k-step t:
     // qb[t][0] = dims (16t+2c, +1), qb[t][1] = dims (16t+2c+8, +9).
@@ -536,10 +541,9 @@ int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __
     P.splits = L.splits;
     P.g = p.d.n_q_heads / p.d.n_kv_heads;
     dim3 grid(L.splits, p.d.n_kv_heads, b.num_requests);
-    if (b.flags & LAZYATTN_KEYS_PREROTATED)
-        decode_bf16_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
-    else
-        decode_bf16_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
+    auto kern = (b.flags & LAZYATTN_KEYS_PREROTATED) ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+    if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.view(), P) != cudaSuccess)
+        return LAZYATTN_ECUDA;
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }
 

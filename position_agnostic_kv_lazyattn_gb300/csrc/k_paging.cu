@@ -71,12 +71,17 @@ __device__ int find_append_entry(const uint64_t* entries, int e0, int e1, int la
 }
 
 // One block per request: append k_new/v_new into the request's tail page.
+// Launched as a programmatic dependent of the previous kernel in the stream
+// (the previous step's attention): it lets its own dependent launch at once
+// and waits for the previous grid before touching the table or the pool.
 template <typename T, bool PREROT>
 __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32_t* entry_offsets,
                                      const T* __restrict__ k_new, const T* __restrict__ v_new, int32_t* qpos) {
     const int r = blockIdx.x;
     __shared__ int s_entry;
     __shared__ uint64_t s_e;
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     if (threadIdx.x < 32) {
         const int e0 = entry_offsets[r], e1 = entry_offsets[r + 1];
         int t = find_append_entry(entries, e0, e1, threadIdx.x);
@@ -105,6 +110,39 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
     const int D = pv.d, half = D / 2;
     T* kp = static_cast<T*>(pv.k_pool);
     T* vp = static_cast<T*>(pv.v_pool);
+    if (sizeof(T) == 2 && half % 8 == 0) {
+        // 16-byte vectors: thread = (kv head, 8 dims of the first half) and
+        // their rotate-half partners; rows are 16-byte aligned (D % 16 == 0,
+        // aligned k_new / v_new / pools)
+        const int g8 = half / 8;
+        for (int i = threadIdx.x; i < pv.hkv * g8; i += blockDim.x) {
+            const int h = i / g8, d = (i % g8) * 8;
+            const size_t src = ((size_t)r * pv.hkv + h) * D;
+            const size_t dst = (((size_t)page * pv.hkv + h) * kPage + slot) * D;
+            uint4 k1 = *reinterpret_cast<const uint4*>(k_new + src + d);
+            uint4 k2 = *reinterpret_cast<const uint4*>(k_new + src + d + half);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(v_new + src + d);
+            const uint4 v2 = *reinterpret_cast<const uint4*>(v_new + src + d + half);
+            if (PREROT) {
+                T a[8], b[8];
+                *reinterpret_cast<uint4*>(a) = k1;
+                *reinterpret_cast<uint4*>(b) = k2;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float2 cs = pv.rope[(size_t)pos * half + d + j];
+                    const float x = to_f(a[j]), y = to_f(b[j]);
+                    a[j] = from_f<T>(x * cs.x - y * cs.y);
+                    b[j] = from_f<T>(x * cs.y + y * cs.x);
+                }
+                k1 = *reinterpret_cast<const uint4*>(a);
+                k2 = *reinterpret_cast<const uint4*>(b);
+            }
+            *reinterpret_cast<uint4*>(kp + dst + d) = k1;
+            *reinterpret_cast<uint4*>(kp + dst + d + half) = k2;
+            *reinterpret_cast<uint4*>(vp + dst + d) = v1;
+            *reinterpret_cast<uint4*>(vp + dst + d + half) = v2;
+        }
+    } else
     for (int i = threadIdx.x; i < pv.hkv * half; i += blockDim.x) {
         const int h = i / half, d = i % half;
         const size_t src = ((size_t)r * pv.hkv + h) * D;
@@ -238,9 +276,10 @@ int launch_decode_append(const lazyattn_pool& p, const lazyattn_batch& b, const 
                                                  static_cast<const float*>(v_new), qpos);
     } else {
         auto kern = pre ? decode_append_kernel<__nv_bfloat16, true> : decode_append_kernel<__nv_bfloat16, false>;
-        kern<<<b.num_requests, 128, 0, stream>>>(pv, b.entries, b.entry_offsets,
-                                                 static_cast<const __nv_bfloat16*>(k_new),
-                                                 static_cast<const __nv_bfloat16*>(v_new), qpos);
+        if (launch_dependent(kern, dim3(b.num_requests), dim3(128), 0, stream, pv, b.entries, b.entry_offsets,
+                             static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+                             qpos) != cudaSuccess)
+            return LAZYATTN_ECUDA;
     }
     return cuda_status();
 }
