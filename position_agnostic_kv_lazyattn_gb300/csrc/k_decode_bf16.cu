@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
     }
     __syncthreads();
+    const int e0 = P.entry_offsets[r], e1 = P.entry_offsets[r + 1];   // not written by the append
     grid_dep_wait();
     const int m = P.qpos[r];
     __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
@@ -172,31 +173,6 @@ __global__ void __launch_bounds__(kThreads, 3)
         return;
     }
 
-    // q of head gr, rotated at m and pre-scaled, as the B operand of k-step t:
-    // qb[t][0] = dims (16t+2c, +1), qb[t][1] = dims (16t+2c+8, +9).
-    uint32_t qb[8][2];
-    if (gr < g) {
-        const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD);
-        const float4* row = reinterpret_cast<const float4*>(pv.rope + (size_t)m * (kD / 2));
-        const float sc = kLog2e * rsqrtf((float)kD);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int d = 16 * t + 2 * c + 8 * hf;
-                const uint32_t x = __ldg(qp + d / 2), y = __ldg(qp + (d + 64) / 2);
-                const float4 cs = __ldg(row + d / 2);
-                const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
-                qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);
-                qb[t + 4][hf] = pack_h2((a0 * cs.y + b0 * cs.x) * sc, (a1 * cs.w + b1 * cs.z) * sc);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
-    }
-
-    const int e0 = P.entry_offsets[r], e1 = P.entry_offsets[r + 1];
     const int chunk = (e1 - e0 + S - 1) / S;
     const int cb = e0 + s * chunk;
     const int ce = min(e1, cb + chunk);
@@ -233,6 +209,31 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
         issue(0, e_cur);
         issue(1, e_n1);
+    }
+
+    // (the first pages are in flight while q is read and rotated)
+    // q of head gr, rotated at m and pre-scaled, as the B operand of k-step t:
+    // qb[t][0] = dims (16t+2c, +1), qb[t][1] = dims (16t+2c+8, +9).
+    uint32_t qb[8][2];
+    if (gr < g) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD);
+        const float4* row = reinterpret_cast<const float4*>(pv.rope + (size_t)m * (kD / 2));
+        const float sc = kLog2e * rsqrtf((float)kD);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int d = 16 * t + 2 * c + 8 * hf;
+                const uint32_t x = __ldg(qp + d / 2), y = __ldg(qp + (d + 64) / 2);
+                const float4 cs = __ldg(row + d / 2);
+                const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
+                qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);
+                qb[t + 4][hf] = pack_h2((a0 * cs.y + b0 * cs.x) * sc, (a1 * cs.w + b1 * cs.z) * sc);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
     }
 
     float o[8][4];
