@@ -115,14 +115,50 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
     return n;
 }
 
-// Rotate a pair of bf16x2 registers holding dims (d, d+1) and (d+64, d+65) by
-// the angles whose (cos, sin) are cs = (c_d, s_d, c_{d+1}, s_{d+1}); fp16x2 out.
-__device__ __forceinline__ void rotate2(uint32_t& x, uint32_t& y, const float4& cs) {
-    const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
-    x = pack_h2(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w);
-    y = pack_h2(a0 * cs.y + b0 * cs.x, a1 * cs.w + b1 * cs.z);
-}
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) { return pack_h2(bf_lo(x), bf_hi(x)); }
+
+// Two fp32 lanes per instruction (packed f32x2 arithmetic).
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "mul.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "sub.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+// Angle addition for two frequencies at once: (c, s) of angle 1 + angle 2.
+__device__ __forceinline__ void compose2(float2 c1, float2 s1, float2 c2, float2 s2, float2& c, float2& s) {
+    c = f2_sub(f2_mul(c1, c2), f2_mul(s1, s2));
+    s = f2_fma(s1, c2, f2_mul(c1, s2));
+}
+// Rotate dims (d, d+1) [bf16x2 x] and their rotate-half partners (d+64, d+65)
+// [bf16x2 y] by angles with cosines c and sines s; fp16x2 out.
+__device__ __forceinline__ void rotate2v(uint32_t& x, uint32_t& y, float2 c, float2 s) {
+    const float2 a = make_float2(bf_lo(x), bf_hi(x)), b = make_float2(bf_lo(y), bf_hi(y));
+    const float2 u = f2_sub(f2_mul(a, c), f2_mul(b, s));
+    const float2 v = f2_fma(a, s, f2_mul(b, c));
+    x = pack_h2(u.x, u.y);
+    y = pack_h2(v.x, v.y);
+}
 
 // 16-byte unit f4 (frequencies 2*f4, 2*f4+1) of slot-table row t. Odd rows swap
 // the two 64-byte halves, so the lanes of a quarter warp (rows 2q and 2q+1,
@@ -159,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int t = i >> 5, f4 = i & 31;
             const float4 v = t < pv.max_position ? __ldg(reinterpret_cast<const float4*>(pv.rope) + t * 32 + f4)
                                                  : make_float4(1.f, 0.f, 1.f, 0.f);
-            slot_tab[slot_unit(t, f4)] = v;
+            slot_tab[slot_unit(t, f4)] = make_float4(v.x, v.z, v.y, v.w);   // (cos, cos, sin, sin)
         }
     }
     __syncthreads();
@@ -253,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         if (nv < 0 && lane == 0) record_error(pv.status, LAZYATTN_ERANGE);
         if (nv > 0) {
             if (!PREROT) {
-                rowbuf[lane] = row_cur;
+                rowbuf[lane] = make_float4(row_cur.x, row_cur.z, row_cur.y, row_cur.w);   // (cos, cos, sin, sin)
                 __syncwarp();
             }
             if (!mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, abort_flag)) break;
@@ -277,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 3)
                         // angle of token gr = angle(start) + angle(gr), and of token gr + 8
                         // = that + angle(8); every factor from a table row
                         const int f4 = 8 * t + c + 4 * hf;
+                        // table entries are (cos, cos, sin, sin) of frequencies 2*f4, 2*f4+1
                         const float4 b4 = rowbuf[f4], x = slot_tab[slot_unit(gr, f4)], y = slot_tab[slot_unit(8, f4)];
-                        const float4 ca = make_float4(b4.x * x.x - b4.y * x.y, b4.y * x.x + b4.x * x.y,
-                                                      b4.z * x.z - b4.w * x.w, b4.w * x.z + b4.z * x.w);
-                        const float4 cb = make_float4(ca.x * y.x - ca.y * y.y, ca.y * y.x + ca.x * y.y,
-                                                      ca.z * y.z - ca.w * y.w, ca.w * y.z + ca.z * y.w);
-                        rotate2(lo[2 * hf], hi[2 * hf], ca);
-                        rotate2(lo[2 * hf + 1], hi[2 * hf + 1], cb);
+                        float2 cac, cas, cbc, cbs;
+                        compose2(make_float2(b4.x, b4.y), make_float2(b4.z, b4.w), make_float2(x.x, x.y),
+                                 make_float2(x.z, x.w), cac, cas);
+                        compose2(cac, cas, make_float2(y.x, y.y), make_float2(y.z, y.w), cbc, cbs);
+                        rotate2v(lo[2 * hf], hi[2 * hf], cac, cas);
+                        rotate2v(lo[2 * hf + 1], hi[2 * hf + 1], cbc, cbs);
                     }
                 } else {
 #pragma unroll
