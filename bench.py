@@ -43,6 +43,37 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# DRAM bytes (read + write) per launch from one ncu capture of this bench's own
+# command on the named workload (summary: profiles/traffic_llama3_8b.md), keyed
+# by a hash of the kernel sources the capture ran; reported only while the
+# sources still hash the same, else null. "decode" = one lazyattn_decode call
+# (append + attention kernels), "prefill" = the prefill kernel.
+KERNEL_SOURCES = {
+    "decode": ["k_decode_bf16.cu", "k_paging.cu", "internal.h", "tc_ptx.cuh"],
+    "prefill": ["k_prefill_tc.cu", "internal.h", "tc_ptx.cuh"],
+}
+NCU_TRAFFIC = {
+    ("llama3_8b", "decode"): (69.35e6, "d20b04487f59fa2d"),
+    ("llama3_8b", "prefill"): (78.13e6, "15537909d79a382a"),
+}
+
+
+def sources_sha(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "position_agnostic_kv_lazyattn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kind):
+    entry = NCU_TRAFFIC.get((workload, kind))
+    if entry is None or entry[1] != sources_sha(kind):
+        return None
+    return entry[0]
+
+
 def work_model(cfg):
     """Algorithmic bytes / FLOPs of one step of cfg (all requests)."""
     R, Hkv, Hq, D = cfg.n_requests, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
@@ -297,10 +328,13 @@ def run_ours(args, rank, world):
         "frac_tensor_peak": round(pre_tflops / world / tc_peak, 4),
         "roofline": {"kernel": "lazyattn_decode (append + split-K attention)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind},
+                     "frac": round(achieved / hbm_peak, 4), "traffic": measured_traffic(cfg.name, "decode"),
+                     "traffic_unit": "bytes per decode call (DRAM read + write, ncu)",
+                     "algorithmic_bytes_per_call": round(per_call_bytes), "peak_kind": peak_kind},
         "prefill_roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(pre_tflops, 2),
                              "peak": tc_peak, "unit": "TFLOP/s", "frac": round(pre_tflops / tc_peak, 4),
-                             "peak_kind": peak_kind},
+                             "traffic": measured_traffic(cfg.name, "prefill"),
+                             "traffic_unit": "bytes per launch (DRAM read + write, ncu)", "peak_kind": peak_kind},
         "materialising_baseline": None if b_mat is None else {
             "materialise_ms": round(b_mat, 4), "ttft_ms": round(b_mat + b_pre, 4), "decode_ms": round(b_dec, 4),
             "decode_gbs": round(dec_total_bytes / (b_dec / 1e3) / 1e9, 1) if b_dec else None,
