@@ -280,6 +280,47 @@ def run_ours(args, rank, world):
         b_pre = statistics.mean(r[1].elapsed_time(r[2]) for r in brec)
         b_dec = statistics.mean(r[2].elapsed_time(r[3]) for r in brec)
 
+    # No-RoPE comparison (the paper's Table 12 experiment): the same kernels on the
+    # same shared pages with rotation switched off (the keys are treated as
+    # already rotated: numerically meaningless, identical data movement), so the
+    # ratio is the cost of rotating at run time.
+    norope = None
+    if not args.no_extras:
+        nb = b.with_entries(b.entries_host, L.LAZYATTN_KEYS_PREROTATED, device=dev)
+        nb_entries0 = nb.entries.clone()
+
+        def prefill_plain():
+            if nb.total_q:
+                L.lazyattn_prefill(env.pool.handle, nb.c, env.q, out_p, None, 0, None)
+
+        def decode_plain():
+            for t in range(cfg.decode_steps):
+                q, k, v = dec_in[t]
+                L.lazyattn_decode(env.pool.handle, nb.c, q, k, v, out_d, ws, ws_bytes, None)
+
+        g_npre = capture(prefill_plain)
+        nb.entries.copy_(nb_entries0)
+        g_ndec = capture(decode_plain)
+        nrec = []
+        for it in range(max(2, min(args.steps, 20)) + 2):
+            nb.entries.copy_(nb_entries0)
+            flush.zero_()
+            e = [ev() for _ in range(3)]
+            e[0].record(stream)
+            g_npre.replay()
+            e[1].record(stream)
+            g_ndec.replay()
+            e[2].record(stream)
+            if it >= 2:
+                nrec.append(e)
+        torch.cuda.synchronize()
+        n_pre = statistics.mean(r[0].elapsed_time(r[1]) for r in nrec)
+        n_dec = statistics.mean(r[1].elapsed_time(r[2]) for r in nrec)
+        norope = {"prefill_ms": round(n_pre, 4), "decode_ms": round(n_dec, 4),
+                  "prefill_overhead": round(local["pre_ms"] / n_pre, 3) if cfg.q_len and n_pre else None,
+                  "decode_overhead": round(local["dec_s"] * 1e3 / n_dec, 3) if cfg.decode_steps and n_dec else None,
+                  "note": "same kernels and pages, rotation off; overhead = lazy time / no-RoPE time"}
+
     # end to end through host buffers (pinned), copies inside the timed region
     e2e = None
     if cfg.decode_steps and not args.no_extras:
@@ -341,6 +382,7 @@ def run_ours(args, rank, world):
             "lazy_ttft_speedup": round((b_mat + b_pre) / local["pre_ms"], 3) if local["pre_ms"] else None,
             "lazy_decode_speedup": round(b_dec / (local["dec_s"] * 1e3), 3) if local["dec_s"] else None,
             "lazy_step_speedup": round((b_mat + b_pre + b_dec) / local["step_ms"], 3)},
+        "norope": norope,
         "e2e": e2e,
         "gpu_launches": args.steps * ((1 if cfg.q_len else 0) + 2 * cfg.decode_steps),
         "wall_s_timed": round(local["wall"], 4),
@@ -375,7 +417,7 @@ def cpu_baseline(cfg, budget_s=15.0, n_steps=None):
     nbytes = 0.0
     esz = 4 if cfg.dtype == "f32" else 2
     done_req = 0
-    steps = n_steps or min(cfg.decode_steps, 2) or 1
+    steps = n_steps or min(cfg.decode_steps, 16) or 1
     for r in range(cfg.n_requests):
         ctx = [workload.doc_kv(cfg, int(d)) for d in docs[r]]
         if cfg.q_len:

@@ -81,6 +81,13 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
  *   rope_table    float2 [max_position][head_dim/2]; filled by lazyattn_pool_create
  *   status_word   one int32 in device memory, zeroed by lazyattn_pool_create; kernels
  *                 record the first device-side error there
+ *   rope_scaling  LAZYATTN_ROPE_* below (0: plain RoPE; the fields after it are then ignored)
+ *   rope_original_max_position   context length the model was trained for (YaRN, Llama 3.1)
+ *   rope_factor   scale factor s >= 1 (all scaled kinds)
+ *   rope_low, rope_high          YaRN: beta_slow, beta_fast (rotations within the original
+ *                 context below which frequencies are interpolated / above which they are
+ *                 kept); Llama 3.1: low_freq_factor, high_freq_factor. rope_low < rope_high.
+ * A zero-initialised descriptor tail means plain RoPE.
  */
 typedef struct lazyattn_pool_desc {
     int32_t num_pages;
@@ -95,7 +102,29 @@ typedef struct lazyattn_pool_desc {
     void* v_pool;
     void* rope_table;
     int32_t* status_word;
+    int32_t rope_scaling;
+    int32_t rope_original_max_position;
+    double rope_factor;
+    double rope_low;
+    double rope_high;
 } lazyattn_pool_desc;
+
+/* RoPE-family variants (§3.5 "Generalization Beyond Standard RoPE": scaled/NTK
+ * variants and YaRN keep the score q^T R_{n-m} k, with variant-specific scaling
+ * metadata). Each changes only the frequencies theta_i of the position table,
+ * plus, for YaRN, an attention temperature on the logits:
+ *   LINEAR  position interpolation: theta_i / s
+ *   NTK     NTK-aware base change: base' = base * s^(D/(D-2))
+ *   YARN    per-frequency ramp between theta_i / s and theta_i by the number r_i
+ *           of rotations within the original context (interpolated for r < low,
+ *           kept for r > high, linear in between); logits times (0.1 ln s + 1)^2
+ *   LLAMA3  the Llama 3.1 rule: wavelength 2 pi / theta_i below orig/high kept,
+ *           above orig/low divided by s, smooth blend in between */
+#define LAZYATTN_ROPE_DEFAULT 0
+#define LAZYATTN_ROPE_LINEAR 1
+#define LAZYATTN_ROPE_NTK 2
+#define LAZYATTN_ROPE_YARN 3
+#define LAZYATTN_ROPE_LLAMA3 4
 
 typedef struct lazyattn_pool* lazyattn_pool_t;
 

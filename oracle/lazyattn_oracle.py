@@ -40,7 +40,7 @@ from typing import Iterable, List, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "PAGE_SIZE", "unpack_entry", "resolve_entries", "rope_inv_freq", "rope",
+    "PAGE_SIZE", "unpack_entry", "resolve_entries", "RopeSpec", "rope_inv_freq", "logit_scale", "rope",
     "attention", "prefill_request", "decode_request", "materialize_rotated",
     "attention_prerotated", "paged_context", "paged_prefill", "paged_decode_step",
 ]
@@ -81,10 +81,73 @@ def resolve_entries(entries: Iterable[int]) -> List[Tuple[int, int, int]]:
 # RoPE
 # ----------------------------------------------------------------------------
 
-def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
-    """theta_i = base^(-2i/D), i = 0 .. D/2-1, fp64."""
+class RopeSpec:
+    """A RoPE base with one of the scaled RoPE-family variants that §3.5
+    ("Generalization Beyond Standard RoPE") says keep the score
+    q^T R_{n-m} k with variant-specific metadata. Each variant, as its
+    publication defines it, changes the frequencies:
+      "linear"  position interpolation (Chen et al., 2023): every frequency
+                divided by the factor s, i.e. positions read as p / s;
+      "ntk"     NTK-aware scaling: the base becomes base * s^(D / (D - 2));
+      "yarn"    YaRN (Peng et al., 2023): with r_i = (original context) /
+                (wavelength 2 pi / theta_i), frequencies with r_i < low are
+                interpolated (theta_i / s), those with r_i > high are kept, a
+                linear ramp in r blends in between; the logits are multiplied
+                by (0.1 ln s + 1)^2 (the attention temperature);
+      "llama3"  the Llama 3.1 rule: wavelengths below original / high kept,
+                above original / low divided by s, and in between a blend with
+                weight (original / wavelength - low) / (high - low) on the
+                kept frequency.
+    """
+
+    def __init__(self, base: float, kind: str = "default", factor: float = 1.0,
+                 original_max_position: int = 0, low: float = 0.0, high: float = 0.0):
+        self.base, self.kind, self.factor = float(base), kind, float(factor)
+        self.original, self.low, self.high = float(original_max_position), float(low), float(high)
+
+    def inv_freq(self, head_dim: int) -> np.ndarray:
+        i = np.arange(head_dim // 2, dtype=np.float64)
+        plain = np.power(self.base, -2.0 * i / head_dim)
+        s = self.factor
+        if self.kind == "default":
+            return plain
+        if self.kind == "linear":
+            return plain / s
+        if self.kind == "ntk":
+            return np.power(self.base * s ** (head_dim / (head_dim - 2.0)), -2.0 * i / head_dim)
+        if self.kind == "yarn":
+            r = self.original / (2.0 * np.pi / plain)
+            ramp = np.clip((r - self.low) / (self.high - self.low), 0.0, 1.0)
+            return (1.0 - ramp) * plain / s + ramp * plain
+        if self.kind == "llama3":
+            wavelength = 2.0 * np.pi / plain
+            blend = (self.original / wavelength - self.low) / (self.high - self.low)
+            mid = (1.0 - blend) * plain / s + blend * plain
+            return np.where(wavelength < self.original / self.high, plain,
+                            np.where(wavelength > self.original / self.low, plain / s, mid))
+        raise ValueError(self.kind)
+
+    def logit_scale(self, head_dim: int) -> float:
+        scale = 1.0 / np.sqrt(np.float64(head_dim))
+        if self.kind == "yarn" and self.factor > 1.0:
+            scale *= (0.1 * np.log(self.factor) + 1.0) ** 2
+        return float(scale)
+
+
+def rope_inv_freq(head_dim: int, theta) -> np.ndarray:
+    """theta_i, i = 0 .. D/2-1, fp64: base^(-2i/D) for a plain base (a number),
+    or the variant's frequencies for a RopeSpec."""
+    if isinstance(theta, RopeSpec):
+        return theta.inv_freq(head_dim)
     i = np.arange(head_dim // 2, dtype=np.float64)
     return np.power(np.float64(theta), -2.0 * i / head_dim)
+
+
+def logit_scale(head_dim: int, theta) -> float:
+    """Scale of q.k in the softmax: 1/sqrt(D) (Eq. 4), times YaRN's temperature."""
+    if isinstance(theta, RopeSpec):
+        return theta.logit_scale(head_dim)
+    return float(1.0 / np.sqrt(np.float64(head_dim)))
 
 
 def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
@@ -105,10 +168,11 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def attention_prerotated(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray,
-                         q_pos: np.ndarray, k_pos: np.ndarray) -> np.ndarray:
+                         q_pos: np.ndarray, k_pos: np.ndarray, scale: float = None) -> np.ndarray:
     """Causal softmax attention over already rotated q and k.
 
-    q_rot: [Lq][Hq][D]; k_rot, v: [L][Hkv][D]; q_pos: [Lq]; k_pos: [L].
+    q_rot: [Lq][Hq][D]; k_rot, v: [L][Hkv][D]; q_pos: [Lq]; k_pos: [L];
+    scale: logit scale, 1/sqrt(D) when None.
     Returns [Lq][Hq][D] fp64.
     """
     q_rot = np.asarray(q_rot, np.float64)
@@ -121,7 +185,7 @@ def attention_prerotated(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray,
     out = np.zeros((Lq, Hq, D), dtype=np.float64)
     for h in range(Hq):
         kv = h // g
-        s = (q_rot[:, h, :] @ k_rot[:, kv, :].T) / np.sqrt(np.float64(D))
+        s = (q_rot[:, h, :] @ k_rot[:, kv, :].T) * (1.0 / np.sqrt(np.float64(D)) if scale is None else scale)
         s = np.where(visible, s, -np.inf)
         m = s.max(axis=1, keepdims=True)
         p = np.exp(s - m)
@@ -137,7 +201,7 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos,
     k_pos = np.asarray(k_pos, dtype=np.int64)
     q_rot = rope(q, q_pos[:, None], theta)
     k_rot = rope(k, k_pos[:, None], theta)
-    return attention_prerotated(q_rot, k_rot, v, q_pos, k_pos)
+    return attention_prerotated(q_rot, k_rot, v, q_pos, k_pos, logit_scale(np.asarray(q).shape[-1], theta))
 
 
 def materialize_rotated(k: np.ndarray, k_pos, theta: float) -> np.ndarray:

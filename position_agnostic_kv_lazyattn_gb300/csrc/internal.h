@@ -62,6 +62,7 @@ struct PoolView {
     int32_t num_pages;
     int32_t max_position;
     int32_t hq, hkv, d;
+    float qk_scale;       // logit scale: 1/sqrt(D), times YaRN's attention temperature
 };
 
 // Record the first device-side error; later ones are dropped.
@@ -101,6 +102,7 @@ struct lazyattn_pool {
     int device = 0;
     int sm_count = 0;
     int decode_slots = 0;              // resident decode CTAs on the whole GPU
+    float qk_scale = 0.f;              // logit scale (1/sqrt(D), YaRN temperature included)
     bool have_maps = false;            // bf16 pools: TMA views of the K and V pools
     CUtensorMap kmap, vmap;
     lazyattn::PoolView view() const;

@@ -19,7 +19,7 @@
 //     bytes to the L2 traffic and no global load waits inside the page loop,
 //   * computes S^T = K' Q'^T with m16n8k16 MMAs (N = the group's <= 8 heads),
 //   * runs the online softmax in the log2 domain (q is pre-scaled by
-//     log2(e)/sqrt(D)),
+//     log2(e) times the logit scale, 1/sqrt(D)),
 //   * accumulates O^T += V^T P^T (V^T fragments from ldmatrix.trans, P^T from
 //     movmatrix).
 // Warps combine through shared memory; splits combine through a partial buffer
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (gr < g) {
         const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD);
         const float4* row = reinterpret_cast<const float4*>(pv.rope + (size_t)m * (kD / 2));
-        const float sc = kLog2e * rsqrtf((float)kD);
+        const float sc = kLog2e * pv.qk_scale;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
 #pragma unroll

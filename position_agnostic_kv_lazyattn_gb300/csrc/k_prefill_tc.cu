@@ -525,10 +525,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_valid = false;
         }
 
-        // Q row: rotate at m_row, scale by log2(e)/sqrt(D), fp16, 128B-swizzled K-major
+        // Q row: rotate at m_row, scale by log2(e) times the pool's logit scale (1/sqrt(D)),
+        // fp16, 128B-swizzled K-major
         {
             uint8_t* qsm = sm + kOffQ + qi * kQBytes;
-            const float sc = kLog2e * rsqrtf((float)kD);
+            const float sc = kLog2e * pv.qk_scale;
             const __nv_bfloat16* qp_ = P.q + ((size_t)(q0 + tok) * Hq + (size_t)h * g + jh) * kD;
             const float* cs = reinterpret_cast<const float*>(pv.rope + (size_t)(row_valid ? m_row : 0) * (kD / 2));
 #pragma unroll 2

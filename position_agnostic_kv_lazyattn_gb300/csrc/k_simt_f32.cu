@@ -46,11 +46,11 @@ __global__ void attention_f32_kernel(PoolView pv, const uint64_t* __restrict__ e
         return;
     }
 
-    // q rotated at its own position m, pre-scaled by 1/sqrt(D)
+    // q rotated at its own position m, pre-scaled by the logit scale (1/sqrt(D))
     float qr[J];
     {
         const float* qp = q + ((size_t)row * pv.hq + h) * D;
-        const float sc = rsqrtf((float)D);
+        const float sc = pv.qk_scale;
 #pragma unroll
         for (int j = 0; j < J / 2; ++j) {
             const int d = lane + 32 * j;

@@ -22,6 +22,7 @@ lazyattn::PoolView lazyattn_pool::view() const {
     v.hq = d.n_q_heads;
     v.hkv = d.n_kv_heads;
     v.d = d.head_dim;
+    v.qk_scale = qk_scale;
     return v;
 }
 
@@ -53,6 +54,52 @@ size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position) {
     return (size_t)max_position * (size_t)(head_dim / 2) * sizeof(float2);
 }
 
+// theta_i, i < D/2, of the pool's RoPE variant (fp64), and the logit scale.
+static void rope_frequencies(const lazyattn_pool_desc& d, double* inv, float* qk_scale) {
+    const int half = d.head_dim / 2;
+    const double D = (double)d.head_dim, s = d.rope_factor, two_pi = 6.283185307179586476925286766559;
+    double base = d.rope_theta;
+    if (d.rope_scaling == LAZYATTN_ROPE_NTK) base *= pow(s, D / (D - 2.0));
+    for (int i = 0; i < half; ++i) {
+        const double th = pow(base, -2.0 * (double)i / D);
+        double out = th;
+        switch (d.rope_scaling) {
+        case LAZYATTN_ROPE_LINEAR:
+            out = th / s;
+            break;
+        case LAZYATTN_ROPE_YARN: {
+            const double r = (double)d.rope_original_max_position * th / two_pi;   // rotations in the original context
+            double gamma = (r - d.rope_low) / (d.rope_high - d.rope_low);
+            gamma = gamma < 0.0 ? 0.0 : (gamma > 1.0 ? 1.0 : gamma);
+            out = (1.0 - gamma) * th / s + gamma * th;
+            break;
+        }
+        case LAZYATTN_ROPE_LLAMA3: {
+            const double wavelen = two_pi / th;
+            const double lo_wl = (double)d.rope_original_max_position / d.rope_low;
+            const double hi_wl = (double)d.rope_original_max_position / d.rope_high;
+            if (wavelen < hi_wl) {
+                out = th;
+            } else if (wavelen > lo_wl) {
+                out = th / s;
+            } else {
+                const double smooth = ((double)d.rope_original_max_position / wavelen - d.rope_low) /
+                                      (d.rope_high - d.rope_low);
+                out = (1.0 - smooth) * th / s + smooth * th;
+            }
+            break;
+        }
+        default:
+            break;
+        }
+        inv[i] = out;
+    }
+    if (d.rope_scaling == LAZYATTN_ROPE_YARN && s > 1.0) {
+        const double t = 0.1 * log(s) + 1.0;
+        *qk_scale = (float)(t * t / sqrt(D));
+    }
+}
+
 int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_pool_t* out_pool) {
     if (!desc || !out_pool) return LAZYATTN_EINVAL;
     *out_pool = nullptr;
@@ -62,6 +109,11 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         d.max_position > LAZYATTN_MAX_START + kPage)
         return LAZYATTN_EINVAL;
     if (!d.k_pool || !d.v_pool || !d.rope_table || !d.status_word) return LAZYATTN_EINVAL;
+    if (d.rope_scaling < LAZYATTN_ROPE_DEFAULT || d.rope_scaling > LAZYATTN_ROPE_LLAMA3) return LAZYATTN_EINVAL;
+    if (d.rope_scaling != LAZYATTN_ROPE_DEFAULT && !(d.rope_factor >= 1.0)) return LAZYATTN_EINVAL;
+    if ((d.rope_scaling == LAZYATTN_ROPE_YARN || d.rope_scaling == LAZYATTN_ROPE_LLAMA3) &&
+        (d.rope_original_max_position < 1 || !(d.rope_low >= 0.0) || !(d.rope_high > d.rope_low)))
+        return LAZYATTN_EINVAL;
     if (!aligned16(d.k_pool) || !aligned16(d.v_pool) || !aligned16(d.rope_table) ||
         (reinterpret_cast<uintptr_t>(d.status_word) & 3u))
         return LAZYATTN_EINVAL;
@@ -98,11 +150,13 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         return LAZYATTN_EINVAL;   // pool too large for 32-bit TMA rows, or no tensor-map support
     }
 
-    // Position table: angle pos * theta^(-2i/D) in fp64, cos/sin in fp64, stored fp32.
+    // Position table: angle pos * theta_i in fp64, cos/sin in fp64, stored fp32;
+    // theta_i from the pool's RoPE variant.
     const int half = d.head_dim / 2;
     std::vector<float2> tab((size_t)d.max_position * (size_t)half);
     std::vector<double> inv(half);
-    for (int i = 0; i < half; ++i) inv[i] = pow(d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
+    p->qk_scale = (float)(1.0 / sqrt((double)d.head_dim));
+    rope_frequencies(d, inv.data(), &p->qk_scale);
     for (int32_t pos = 0; pos < d.max_position; ++pos) {
         float2* row = &tab[(size_t)pos * half];
         for (int i = 0; i < half; ++i) {

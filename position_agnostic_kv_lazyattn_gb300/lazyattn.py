@@ -20,6 +20,11 @@ LAZYATTN_BF16 = 1
 LAZYATTN_KEYS_PREROTATED = 1
 LAZYATTN_OP_PREFILL = 0
 LAZYATTN_OP_DECODE = 1
+LAZYATTN_ROPE_DEFAULT = 0
+LAZYATTN_ROPE_LINEAR = 1
+LAZYATTN_ROPE_NTK = 2
+LAZYATTN_ROPE_YARN = 3
+LAZYATTN_ROPE_LLAMA3 = 4
 
 STATUS = {
     0: "LAZYATTN_OK", -1: "LAZYATTN_EINVAL", -2: "LAZYATTN_ENOSPC", -3: "LAZYATTN_ERANGE",
@@ -41,6 +46,8 @@ class lazyattn_pool_desc(ctypes.Structure):
         ("rope_theta", ctypes.c_double), ("max_position", ctypes.c_int32),
         ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("rope_table", ctypes.c_void_p),
         ("status_word", ctypes.c_void_p),
+        ("rope_scaling", ctypes.c_int32), ("rope_original_max_position", ctypes.c_int32),
+        ("rope_factor", ctypes.c_double), ("rope_low", ctypes.c_double), ("rope_high", ctypes.c_double),
     ]
 
 

@@ -39,7 +39,10 @@ class Segment:
 
 class DevicePool:
     def __init__(self, num_pages: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: str,
-                 rope_theta: float, max_position: int, device="cuda", stream=None):
+                 rope_theta: float, max_position: int, device="cuda", stream=None, rope_scaling=None):
+        """rope_scaling: None (plain RoPE) or a dict with "kind" in {"linear", "ntk",
+        "yarn", "llama3"}, "factor" and, for yarn / llama3, "original_max_position",
+        "low", "high" (see lazyattn.h)."""
         self.dtype = dtype
         self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
@@ -56,6 +59,14 @@ class DevicePool:
                                          float(rope_theta), max_position, self.k_pool.data_ptr(),
                                          self.v_pool.data_ptr(), self.rope_table.data_ptr(),
                                          self.status.data_ptr())
+        if rope_scaling:
+            kinds = {"linear": L.LAZYATTN_ROPE_LINEAR, "ntk": L.LAZYATTN_ROPE_NTK, "yarn": L.LAZYATTN_ROPE_YARN,
+                     "llama3": L.LAZYATTN_ROPE_LLAMA3}
+            self.desc.rope_scaling = kinds[rope_scaling["kind"]]
+            self.desc.rope_factor = float(rope_scaling["factor"])
+            self.desc.rope_original_max_position = int(rope_scaling.get("original_max_position", 0))
+            self.desc.rope_low = float(rope_scaling.get("low", 0.0))
+            self.desc.rope_high = float(rope_scaling.get("high", 0.0))
         self.handle = L.lazyattn_pool_create(self.desc, stream)
 
     def close(self):

@@ -341,13 +341,13 @@ def test_mutant_scale_and_grouping_are_caught(monkeypatch):
     import oracle.lazyattn_oracle as lo
     real = lo.attention_prerotated
 
-    def no_scale(q_rot, k_rot, v, q_pos, k_pos):
-        return real(np.asarray(q_rot) * math.sqrt(q_rot.shape[-1]), k_rot, v, q_pos, k_pos)
+    def no_scale(q_rot, k_rot, v, q_pos, k_pos, scale=None):
+        return real(np.asarray(q_rot) * math.sqrt(q_rot.shape[-1]), k_rot, v, q_pos, k_pos, scale)
 
-    def wrong_group(q_rot, k_rot, v, q_pos, k_pos):
+    def wrong_group(q_rot, k_rot, v, q_pos, k_pos, scale=None):
         Hq, Hkv = q_rot.shape[1], k_rot.shape[1]
         heads = [real(q_rot[:, h:h + 1], k_rot[:, h % Hkv:h % Hkv + 1], v[:, h % Hkv:h % Hkv + 1],
-                      q_pos, k_pos) for h in range(Hq)]
+                      q_pos, k_pos, scale) for h in range(Hq)]
         return np.concatenate(heads, axis=1)
 
     for m in (no_scale, wrong_group):

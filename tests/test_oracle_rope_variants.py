@@ -1,0 +1,94 @@
+"""Pins of the oracle's RoPE-family variants (§3.5 "RoPE-family variants":
+scaled/NTK and YaRN keep the score form with variant-specific metadata).
+
+Each variant is checked against what its definition fixes independently of the
+oracle's own formula: linear scaling is RoPE at interpolated positions p / s;
+NTK-aware scaling keeps the highest frequency and divides the lowest by exactly
+s; YaRN and the Llama 3.1 rule keep the high-frequency band, interpolate the
+low-frequency band and blend monotonically in between, and reduce to plain RoPE
+at s = 1; YaRN's logit scale is (0.1 ln s + 1)^2 / sqrt(D).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import RopeSpec
+
+D = 128
+BASE = 5.0e5
+
+
+def test_linear_is_rope_at_interpolated_positions():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((7, 3, D))
+    pos = np.array([0, 1, 5, 100, 4095, 20000, 65535])[:, None]
+    for s in (2.0, 4.0, 8.0):
+        got = oracle.rope(x, pos, RopeSpec(BASE, "linear", s))
+        want = oracle.rope(x, pos / s, BASE)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_ntk_closed_form():
+    for s in (2.0, 8.0, 32.0):
+        f = RopeSpec(BASE, "ntk", s).inv_freq(D)
+        plain = RopeSpec(BASE).inv_freq(D)
+        assert f[0] == 1.0 and plain[0] == 1.0
+        # lowest frequency: (base * s^(D/(D-2)))^(-(D-2)/D) = base^(-(D-2)/D) / s
+        np.testing.assert_allclose(f[-1], BASE ** (-(D - 2) / D) / s, rtol=1e-13)
+        assert np.all(np.diff(f) < 0)
+        assert np.all(f <= plain) and np.all(f[1:] < plain[1:])
+
+
+@pytest.mark.parametrize("kind,orig,low,high", [("yarn", 4096, 1.0, 32.0), ("llama3", 8192, 1.0, 4.0)])
+def test_band_limits_and_monotone_blend(kind, orig, low, high):
+    s = 8.0
+    plain = RopeSpec(BASE).inv_freq(D)
+    f = RopeSpec(BASE, kind, s, orig, low, high).inv_freq(D)
+    wavelength = 2 * np.pi / plain
+    if kind == "yarn":
+        r = orig / wavelength                  # rotations within the original context
+        keep, interp = r > high, r < low
+    else:
+        keep, interp = wavelength < orig / high, wavelength > orig / low
+    mid = ~keep & ~interp
+    assert keep.any() and interp.any() and mid.any()
+    np.testing.assert_array_equal(f[keep], plain[keep])
+    np.testing.assert_allclose(f[interp], plain[interp] / s, rtol=1e-15)
+    assert np.all(f[mid] < plain[mid]) and np.all(f[mid] > plain[mid] / s)
+    assert np.all(np.diff(f) < 0)             # ordering of the frequencies survives
+    # at s = 1 every variant is plain RoPE
+    np.testing.assert_allclose(RopeSpec(BASE, kind, 1.0, orig, low, high).inv_freq(D), plain, rtol=1e-15)
+
+
+def test_yarn_logit_scale():
+    for s in (1.0, 4.0, 16.0):
+        spec = RopeSpec(BASE, "yarn", s, 4096, 1.0, 32.0)
+        t = 0.1 * np.log(s) + 1.0 if s > 1 else 1.0
+        assert spec.logit_scale(D) == pytest.approx(t * t / np.sqrt(D), rel=1e-15)
+    assert RopeSpec(BASE, "llama3", 8.0, 8192, 1.0, 4.0).logit_scale(D) == pytest.approx(1 / np.sqrt(D))
+
+
+def test_default_spec_matches_plain_base():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((4, 4, D))
+    k = rng.standard_normal((9, 2, D))
+    v = rng.standard_normal((9, 2, D))
+    a = oracle.attention(q, k, v, np.arange(5, 9), np.arange(9), BASE)
+    b = oracle.attention(q, k, v, np.arange(5, 9), np.arange(9), RopeSpec(BASE))
+    np.testing.assert_array_equal(a, b)
+
+
+def test_yarn_temperature_enters_the_logits():
+    """Attention with YaRN equals attention over the same rotations with the
+    logits multiplied by the temperature (checked by brute force)."""
+    rng = np.random.default_rng(2)
+    spec = RopeSpec(BASE, "yarn", 8.0, 4096, 1.0, 32.0)
+    q = rng.standard_normal((1, 1, D))
+    k = rng.standard_normal((6, 1, D))
+    v = rng.standard_normal((6, 1, D))
+    got = oracle.attention(q, k, v, [5], np.arange(6), spec)[0, 0]
+    qr = oracle.rope(q[0, 0], 5, spec)
+    logits = np.array([qr @ oracle.rope(k[j, 0], j, spec) for j in range(6)]) * spec.logit_scale(D)
+    p = np.exp(logits - logits.max())
+    want = (p / p.sum()) @ v[:, 0, :]
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
