@@ -149,7 +149,8 @@ def run_ours(args, rank, world):
     if args.requests:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_requests=min(args.requests, cfg.n_requests))
-    env = wdev.setup(cfg, baseline=not args.no_extras)
+    doc_local = args.keys == "doc_local"
+    env = wdev.setup(cfg, baseline=not args.no_extras and not doc_local, key_storage=args.keys)
     R = cfg.n_requests
     b = env.batch
     stream = torch.cuda.current_stream()
@@ -165,8 +166,9 @@ def run_ours(args, rank, world):
     entries0 = b.entries.clone()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # > 129 MB L2
 
-    # materialising baseline: private copies of every entry's page
-    if not args.no_extras:
+    # materialising baseline: private copies of every entry's page (position-free
+    # pools only: doc-local keys are already rotated)
+    if not args.no_extras and not doc_local:
         base_pages = env.pool.alloc_pages(len(b.entries_host))
         dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.array(base_pages, np.uint64)
         dst_dev = torch.from_numpy(dst.view(np.int64).copy()).to(dev)
@@ -256,7 +258,7 @@ def run_ours(args, rank, world):
 
     # baseline (same box, same inputs): materialise, prefill and decode on private rotated copies
     b_mat = b_pre = b_dec = None
-    if not args.no_extras:
+    if not args.no_extras and not doc_local:
         g_bmat = capture(materialize_base)
         g_bpre = capture(prefill_base)
         mb.entries.copy_(mb_entries0)
@@ -285,7 +287,7 @@ def run_ours(args, rank, world):
     # already rotated: numerically meaningless, identical data movement), so the
     # ratio is the cost of rotating at run time.
     norope = None
-    if not args.no_extras:
+    if not args.no_extras and not doc_local:
         nb = b.with_entries(b.entries_host, L.LAZYATTN_KEYS_PREROTATED, device=dev)
         nb_entries0 = nb.entries.clone()
 
@@ -361,7 +363,8 @@ def run_ours(args, rank, world):
                    "doc_len": cfg.doc_len, "pool_docs": cfg.n_docs, "q_heads": cfg.n_q_heads,
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "query_len": cfg.q_len,
                    "decode_steps": cfg.decode_steps, "zipf_alpha": cfg.zipf_alpha, "seed": cfg.seed,
-                   "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}"},
+                   "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
+                   "keys": args.keys},
         "prefill_tflops": round(pre_tflops, 2), "ttft_ms": round(local["pre_ms"], 4),
         "decode_ms_per_token_step": round(mean_call, 4),
         "timing": "CUDA events around CUDA-graph replays (prefill graph; graph of all decode steps)",
@@ -472,6 +475,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the baseline and end-to-end legs")
     ap.add_argument("--requests", type=int, default=0, help="use only the first N requests (profiling captures)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--keys", default="position_free", choices=["position_free", "doc_local"],
+                    help="key layout: stored without RoPE (default) or rotated at document-local positions")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

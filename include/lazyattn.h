@@ -87,7 +87,13 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
  *   rope_low, rope_high          YaRN: beta_slow, beta_fast (rotations within the original
  *                 context below which frequencies are interpolated / above which they are
  *                 kept); Llama 3.1: low_freq_factor, high_freq_factor. rope_low < rope_high.
- * A zero-initialised descriptor tail means plain RoPE.
+ *   key_storage   LAZYATTN_KEYS_POSITION_FREE (0): K is stored with no position and rotated
+ *                 in the kernels at each key's logical position. LAZYATTN_KEYS_DOC_LOCAL
+ *                 (bf16 pools only): the paper's own layout (§3.2): lazyattn_store_doc
+ *                 stores K rotated at document-local positions (token i of the call at i),
+ *                 prefill applies one relative rotation by the document's offset, decode
+ *                 rotates q instead of the keys; batches must then carry entry_delta.
+ * A zero-initialised descriptor tail means plain RoPE and position-free keys.
  */
 typedef struct lazyattn_pool_desc {
     int32_t num_pages;
@@ -107,7 +113,11 @@ typedef struct lazyattn_pool_desc {
     double rope_factor;
     double rope_low;
     double rope_high;
+    int32_t key_storage;
 } lazyattn_pool_desc;
+
+#define LAZYATTN_KEYS_POSITION_FREE 0
+#define LAZYATTN_KEYS_DOC_LOCAL 1
 
 /* RoPE-family variants (§3.5 "Generalization Beyond Standard RoPE": scaled/NTK
  * variants and YaRN keep the score q^T R_{n-m} k, with variant-specific scaling
@@ -139,7 +149,12 @@ typedef struct lazyattn_pool* lazyattn_pool_t;
  *   q_offsets      prefill: int32 [R+1], request r owns rows [q_offsets[r], q_offsets[r+1]) of q/out
  *   q_start        prefill: int32 [R], logical position of request r's first query row;
  *                  row i of the request sits at q_start[r] + i
- *   flags          0 or LAZYATTN_KEYS_PREROTATED
+ *   flags          0 or LAZYATTN_KEYS_PREROTATED (not with doc-local pools)
+ *   entry_delta    doc-local pools only (else ignored, may be NULL): int32 per entry, the
+ *                  logical position of local position 0 of the entry's document, so the
+ *                  entry's slot j sits at logical start + j and local start - delta + j;
+ *                  0 <= delta <= start. Decode-appended tokens take the local position of
+ *                  their slot in the entry they go into.
  */
 typedef struct lazyattn_batch {
     int32_t num_requests;
@@ -151,6 +166,7 @@ typedef struct lazyattn_batch {
     const int32_t* q_offsets;
     const int32_t* q_start;
     int32_t flags;
+    const int32_t* entry_delta;
 } lazyattn_batch;
 
 #define LAZYATTN_OP_PREFILL 0

@@ -26,6 +26,8 @@
 // in the workspace, reduced by the last CTA of each (r, h) to arrive (atomic
 // ticket, nobody waits). Every wait on a TMA is bounded; on a timeout the warp
 // drains its copies and the CTA records LAZYATTN_EDEVICE.
+#include <limits.h>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -59,6 +61,7 @@ struct DecodeParams {
     float* acc;
     int splits;
     int g;
+    const int32_t* entry_delta;   // doc-local pools: document offset of each entry
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -165,10 +168,15 @@ __device__ __forceinline__ void rotate2v(uint32_t& x, uint32_t& y, float2 c, flo
 // four consecutive units each) hit eight different bank groups.
 __device__ __forceinline__ int slot_unit(int t, int f4) { return t * (kRowBytes / 16) + (f4 ^ ((t & 1) << 2)); }
 
-template <bool PREROT>
+// PREROT: keys already rotated at their logical positions. LOCAL: keys rotated
+// at document-local positions; instead of the keys, q is rotated at m - delta
+// (its position relative to the page's document), once per change of delta
+// (§3.2 "Decoding": rotate q per document rather than K per token).
+template <bool PREROT, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        PoolView pv, DecodeParams P) {
+    constexpr bool ROT_K = !PREROT && !LOCAL;   // keys rotated here
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_full[kWarps][kStages];
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         mbar_fence_init();
     }
     float4* slot_tab = reinterpret_cast<float4*>(sm + kSlotTableOff);   // row t: (cos, sin)(t * theta_i)
-    if (!PREROT) {
+    if (ROT_K) {
         for (int i = tid; i < kSlotRows * 32; i += kThreads) {
             const int t = i >> 5, f4 = i & 31;
             const float4 v = t < pv.max_position ? __ldg(reinterpret_cast<const float4*>(pv.rope) + t * 32 + f4)
@@ -217,9 +225,15 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t ring = smem_u32(sm + warp * kStages * kStageBytes);
     volatile int* abort_flag = &s_abort;
 
-    auto issue = [&](int i, uint64_t e) {   // lane 0 only; e = entry of page i
+    // keys of a page that take part (LOCAL: also a valid document offset d)
+    auto page_n = [&](uint64_t e, int d) {
+        const int n = usable_tokens(pv, e);
+        if (LOCAL && n > 0 && (d < 0 || d > entry_start(e) || m - d < 0 || m - d >= pv.max_position)) return -1;
+        return n;
+    };
+    auto issue = [&](int i, uint64_t e, int d) {   // lane 0 only; e, d = entry and offset of page i
         if (i >= n_w) return;
-        if (usable_tokens(pv, e) <= 0) return;
+        if (page_n(e, d) <= 0) return;
         const int st = i % kStages;
         const uint32_t bar = smem_u32(&bar_full[warp][st]);
         const int y = ((int)entry_page(e) * Hkv + h) * kPage;
@@ -234,24 +248,42 @@ __global__ void __launch_bounds__(kThreads, 3)
     // page ahead (one float4 per lane, staged in the warp's row buffer when
     // the page comes up), so no global load latency sits inside the page loop.
     auto entry_at = [&](int i) { return i < n_w ? my_entries[kWarps * i] : 0ull; };
-    auto row_of = [&](uint64_t e) {
-        return (!PREROT && usable_tokens(pv, e) > 0)
-                   ? __ldg(reinterpret_cast<const float4*>(pv.rope + (size_t)entry_start(e) * (kD / 2)) + lane)
+    auto delta_at = [&](int i) { return (LOCAL && i < n_w) ? P.entry_delta[cb + warp + kWarps * i] : 0; };
+    // the page's row of the position table: its start (ROT_K) or m - delta (LOCAL)
+    auto row_of = [&](uint64_t e, int d) {
+        const int pos = LOCAL ? m - d : entry_start(e);
+        return (!PREROT && page_n(e, d) > 0)
+                   ? __ldg(reinterpret_cast<const float4*>(pv.rope + (size_t)pos * (kD / 2)) + lane)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float4* rowbuf = reinterpret_cast<float4*>(sm + kBaseBufOff + warp * kRowBytes);
     uint64_t e_cur = entry_at(0), e_n1 = entry_at(1);
-    float4 row_next = row_of(e_cur);
+    int d_cur = delta_at(0), d_n1 = delta_at(1);
+    float4 row_next = row_of(e_cur, d_cur);
     if (lane == 0) {
-        issue(0, e_cur);
-        issue(1, e_n1);
+        issue(0, e_cur, d_cur);
+        issue(1, e_n1, d_n1);
     }
 
     // (the first pages are in flight while q is read and rotated)
     // q of head gr, rotated at m and pre-scaled, as the B operand of k-step t:
     // qb[t][0] = dims (16t+2c, +1), qb[t][1] = dims (16t+2c+8, +9).
     uint32_t qb[8][2];
-    if (gr < g) {
+    uint32_t qx[4][2], qy[4][2];   // LOCAL: q as given (bf16 pairs), rotated per document below
+    int last_delta = INT_MIN;
+    if (LOCAL) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + min(gr, g - 1)) * kD);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int d = 16 * t + 2 * c + 8 * hf;
+                qx[t][hf] = gr < g ? __ldg(qp + d / 2) : 0u;
+                qy[t][hf] = gr < g ? __ldg(qp + (d + 64) / 2) : 0u;
+            }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
+    } else if (gr < g) {
         const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + gr) * kD);
         const float4* row = reinterpret_cast<const float4*>(pv.rope + (size_t)m * (kD / 2));
         const float sc = kLog2e * pv.qk_scale;
@@ -281,16 +313,35 @@ __global__ void __launch_bounds__(kThreads, 3)
 
     for (int i = 0; i < n_w; ++i) {
         const uint64_t e = e_cur;
+        const int d = d_cur;
         const uint64_t e_n2 = entry_at(i + 2);
+        const int d_n2 = delta_at(i + 2);
         const float4 row_cur = row_next;
-        row_next = row_of(e_n1);
-        const int nv = usable_tokens(pv, e);
+        row_next = row_of(e_n1, d_n1);
+        const int nv = page_n(e, d);
         const int st = i % kStages;
         if (nv < 0 && lane == 0) record_error(pv.status, LAZYATTN_ERANGE);
         if (nv > 0) {
-            if (!PREROT) {
+            if (ROT_K || (LOCAL && d != last_delta)) {
                 rowbuf[lane] = make_float4(row_cur.x, row_cur.z, row_cur.y, row_cur.w);   // (cos, cos, sin, sin)
                 __syncwarp();
+            }
+            if (LOCAL && d != last_delta) {   // q rotated at m - d, pre-scaled
+                last_delta = d;
+                const float sc = kLog2e * pv.qk_scale;
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const float4 b4 = rowbuf[8 * t + c + 4 * hf];
+                        const float2 a = make_float2(bf_lo(qx[t][hf]), bf_hi(qx[t][hf]));
+                        const float2 b = make_float2(bf_lo(qy[t][hf]), bf_hi(qy[t][hf]));
+                        const float2 cc = make_float2(b4.x * sc, b4.y * sc), ss = make_float2(b4.z * sc, b4.w * sc);
+                        const float2 u = f2_sub(f2_mul(a, cc), f2_mul(b, ss));
+                        const float2 v = f2_fma(a, ss, f2_mul(b, cc));
+                        qb[t][hf] = pack_h2(u.x, u.y);
+                        qb[t + 4][hf] = pack_h2(v.x, v.y);
+                    }
             }
             if (!mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, abort_flag)) break;
             phases ^= 1u << st;
@@ -307,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 const int row = lane & 15, unit = (t & 3) * 2 + (lane >> 4);
                 ldsm_x4(lo, stg + row * 128 + ((unit ^ (row & 7)) << 4));
                 ldsm_x4(hi, stg + 2048 + row * 128 + ((unit ^ (row & 7)) << 4));
-                if (!PREROT) {
+                if (ROT_K) {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         // angle of token gr = angle(start) + angle(gr), and of token gr + 8
@@ -390,17 +441,19 @@ __global__ void __launch_bounds__(kThreads, 3)
         __syncwarp();
         if (lane == 0) {
             fence_proxy_async_smem();   // this warp's reads of the stage precede the next TMA into it
-            issue(i + kStages, e_n2);
+            issue(i + kStages, e_n2, d_n2);
         }
         e_cur = e_n1;
         e_n1 = e_n2;
+        d_cur = d_n1;
+        d_n1 = d_n2;
     }
     if (*abort_flag && lane == 0) {
         // drain copies this warp issued but did not consume before the CTA releases its smem
         volatile int never = 0;
         for (int i = consumed_upto + 1; i < min(n_w, consumed_upto + 1 + kStages); ++i) {
             const uint64_t e = my_entries[kWarps * i];
-            if (usable_tokens(pv, e) <= 0) continue;
+            if (page_n(e, delta_at(i)) <= 0) continue;
             const int st = i % kStages;
             mbar_wait(smem_u32(&bar_full[warp][st]), (phases >> st) & 1u, &never);
             phases ^= 1u << st;
@@ -538,12 +591,14 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 int decode_occupancy(int* ctas_per_sm) {
-    if (cudaFuncSetAttribute(decode_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(decode_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(decode_bf16_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_bf16_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_bf16_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
         return LAZYATTN_ECUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false>, kThreads,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false, false>, kThreads,
                                                          kSmemBytes) == cudaSuccess
                ? LAZYATTN_OK
                : LAZYATTN_ECUDA;
@@ -579,7 +634,10 @@ int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __
     P.splits = L.splits;
     P.g = p.d.n_q_heads / p.d.n_kv_heads;
     dim3 grid(L.splits, p.d.n_kv_heads, b.num_requests);
-    auto kern = (b.flags & LAZYATTN_KEYS_PREROTATED) ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+    P.entry_delta = b.entry_delta;
+    auto kern = p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL
+                    ? decode_bf16_kernel<false, true>
+                    : ((b.flags & LAZYATTN_KEYS_PREROTATED) ? decode_bf16_kernel<true, false> : decode_bf16_kernel<false, false>);
     if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.view(), P) != cudaSuccess)
         return LAZYATTN_ECUDA;
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;

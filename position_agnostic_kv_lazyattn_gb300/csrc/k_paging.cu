@@ -50,6 +50,49 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
     }
 }
 
+// Doc-local pools (bf16): as store_pages_kernel, with K rotated at the token's
+// position within the stored run (its document-local position, §3.2: a
+// document's cache is encoded from position 0). Thread = (slot, 8 dims of the
+// first half) and their rotate-half partners.
+__global__ void store_pages_local_kernel(const __nv_bfloat16* __restrict__ k, const uint4* __restrict__ v,
+                                         __nv_bfloat16* kp, uint4* vp, const float2* rope, int32_t n_tokens,
+                                         int32_t first_page_index, PageList pages, int hkv, int D) {
+    const int j = blockIdx.x, h = blockIdx.y;
+    const int32_t page = pages.ids[j];
+    const int tok0 = (first_page_index + j) * kPage;
+    const int half = D / 2, g8 = half / 8, row_vecs = D / 8;
+    const size_t dst_rows = ((size_t)page * hkv + h) * kPage;
+    for (int i = threadIdx.x; i < kPage * g8; i += blockDim.x) {
+        const int slot = i / g8, d = (i % g8) * 8;
+        const int tok = tok0 + slot;
+        __nv_bfloat16* krow = kp + (dst_rows + slot) * D;
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (tok < n_tokens) {
+            const __nv_bfloat16* src = k + ((size_t)tok * hkv + h) * D;
+            __nv_bfloat16 x[8], y[8];
+            *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(src + d);
+            *reinterpret_cast<uint4*>(y) = *reinterpret_cast<const uint4*>(src + d + half);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float2 cs = rope[(size_t)tok * half + d + t];
+                const float p = __bfloat162float(x[t]), q = __bfloat162float(y[t]);
+                x[t] = __float2bfloat16_rn(p * cs.x - q * cs.y);
+                y[t] = __float2bfloat16_rn(p * cs.y + q * cs.x);
+            }
+            a = *reinterpret_cast<uint4*>(x);
+            b = *reinterpret_cast<uint4*>(y);
+        }
+        *reinterpret_cast<uint4*>(krow + d) = a;
+        *reinterpret_cast<uint4*>(krow + d + half) = b;
+    }
+    for (int i = threadIdx.x; i < kPage * row_vecs; i += blockDim.x) {
+        const int slot = i / row_vecs, c = i % row_vecs;
+        const int tok = tok0 + slot;
+        vp[(dst_rows + slot) * row_vecs + c] = tok < n_tokens ? v[((size_t)tok * hkv + h) * row_vecs + c]
+                                                                : make_uint4(0, 0, 0, 0);
+    }
+}
+
 // Find the append slot of request r: the first entry with nvalid < 16 in the
 // trailing run of writable entries. One warp scans 32 entries per step from
 // the end of the request's entries. Returns the entry index or -1 (all lanes).
@@ -74,9 +117,14 @@ __device__ int find_append_entry(const uint64_t* entries, int e0, int e1, int la
 // Launched as a programmatic dependent of the previous kernel in the stream
 // (the previous step's attention): it lets its own dependent launch at once
 // and waits for the previous grid before touching the table or the pool.
-template <typename T, bool PREROT>
+// MODE: 0 stores k as given (position-free keys); 1 rotates it at its logical
+// position (pre-rotated pages of the materialising baseline); 2 at its
+// document-local position, logical - entry_delta (doc-local pools).
+template <typename T, int MODE>
 __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32_t* entry_offsets,
-                                     const T* __restrict__ k_new, const T* __restrict__ v_new, int32_t* qpos) {
+                                     const T* __restrict__ k_new, const T* __restrict__ v_new, int32_t* qpos,
+                                     const int32_t* entry_delta) {
+    constexpr bool PREROT = MODE != 0;
     const int r = blockIdx.x;
     __shared__ int s_entry;
     __shared__ uint64_t s_e;
@@ -106,7 +154,15 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
     const uint64_t e = s_e;
     const uint32_t page = entry_page(e);
     const int slot = entry_nvalid(e);
-    const int pos = entry_start(e) + slot;
+    int pos = entry_start(e) + slot;
+    if (MODE == 2) {   // rotate at the local position instead
+        const int delta = entry_delta[s_entry];
+        if (delta < 0 || delta > entry_start(e)) {
+            if (threadIdx.x == 0) record_error(pv.status, LAZYATTN_ERANGE);
+            return;
+        }
+        pos -= delta;
+    }
     const int D = pv.d, half = D / 2;
     T* kp = static_cast<T*>(pv.k_pool);
     T* vp = static_cast<T*>(pv.v_pool);
@@ -258,9 +314,15 @@ int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int
         PageList pl;
         for (int i = 0; i < cnt; ++i) pl.ids[i] = pages_host[first + i];
         dim3 grid(cnt, p.d.n_kv_heads);
-        store_pages_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-                                                     static_cast<uint4*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
-                                                     n_tokens, first, pl, p.d.n_kv_heads, row_vecs);
+        if (p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL)
+            store_pages_local_kernel<<<grid, 128, 0, stream>>>(
+                static_cast<const __nv_bfloat16*>(k), static_cast<const uint4*>(v),
+                static_cast<__nv_bfloat16*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
+                static_cast<const float2*>(p.d.rope_table), n_tokens, first, pl, p.d.n_kv_heads, p.d.head_dim);
+        else
+            store_pages_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                                         static_cast<uint4*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
+                                                         n_tokens, first, pl, p.d.n_kv_heads, row_vecs);
         if (cuda_status() != LAZYATTN_OK) return LAZYATTN_ECUDA;
     }
     return LAZYATTN_OK;
@@ -269,16 +331,18 @@ int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int
 int launch_decode_append(const lazyattn_pool& p, const lazyattn_batch& b, const void* k_new, const void* v_new,
                          int32_t* qpos, cudaStream_t stream) {
     const bool pre = (b.flags & LAZYATTN_KEYS_PREROTATED) != 0;
+    const bool local = p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL;
     const PoolView pv = p.view();
     if (p.d.dtype == LAZYATTN_F32) {
-        auto kern = pre ? decode_append_kernel<float, true> : decode_append_kernel<float, false>;
+        auto kern = pre ? decode_append_kernel<float, 1> : decode_append_kernel<float, 0>;
         kern<<<b.num_requests, 128, 0, stream>>>(pv, b.entries, b.entry_offsets, static_cast<const float*>(k_new),
-                                                 static_cast<const float*>(v_new), qpos);
+                                                 static_cast<const float*>(v_new), qpos, nullptr);
     } else {
-        auto kern = pre ? decode_append_kernel<__nv_bfloat16, true> : decode_append_kernel<__nv_bfloat16, false>;
+        auto kern = local ? decode_append_kernel<__nv_bfloat16, 2>
+                          : (pre ? decode_append_kernel<__nv_bfloat16, 1> : decode_append_kernel<__nv_bfloat16, 0>);
         if (launch_dependent(kern, dim3(b.num_requests), dim3(128), 0, stream, pv, b.entries, b.entry_offsets,
                              static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
-                             qpos) != cudaSuccess)
+                             qpos, b.entry_delta) != cudaSuccess)
             return LAZYATTN_ECUDA;
     }
     return cuda_status();

@@ -93,6 +93,7 @@ struct PrefillParams {
     int32_t total_q;
     int32_t g;
     int32_t oob_row;     // a row index outside the K/V tensor maps: TMA fills zeros
+    const int32_t* entry_delta;   // doc-local pools: document offset of each entry
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -153,7 +154,10 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
     return n;
 }
 
-template <bool PREROT>
+// PREROT: keys already rotated at their logical positions (no rotation).
+// LOCAL: keys rotated at document-local positions; each page takes one relative
+// rotation by its document's offset (§3.2 "Prefilling": R_delta R_t = R_(delta+t)).
+template <bool PREROT, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, PoolView pv,
                       PrefillParams P) {
@@ -229,28 +233,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A tile is live iff one of its pages holds a key at a position <= the
         // largest query position of the CTA.
         if (lane == 0 && T > 0) {
-            auto load_entries = [&](int jj, uint64_t (&e)[kPagesPerTile]) {
+            auto load_entries = [&](int jj, uint64_t (&e)[kPagesPerTile], int (&dl)[kPagesPerTile]) {
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     const int idx = e0 + jj * kPagesPerTile + p;
                     const uint64_t v = P.entries[min(idx, e1 - 1)];
                     e[p] = idx < e1 ? v : 0ull;   // 0: an empty entry
+                    if (LOCAL) dl[p] = P.entry_delta[min(idx, e1 - 1)];
                 }
             };
             int last_k[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s) last_k[s] = -1;
             uint64_t cur[kPagesPerTile], nxt[kPagesPerTile] = {};
-            load_entries(0, cur);
+            int curd[kPagesPerTile] = {}, nxtd[kPagesPerTile] = {};   // LOCAL: document offsets
+            load_entries(0, cur, curd);
             int k = 0;
             bool ok = true;
             for (int j = 0; j <= T; ++j) {
-                if (j + 1 < T) load_entries(j + 1, nxt);
+                if (j + 1 < T) load_entries(j + 1, nxt, nxtd);
                 int n[kPagesPerTile];
                 bool live = false;
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     n[p] = j < T ? usable_tokens(pv, cur[p]) : 0;
+                    if (LOCAL && n[p] > 0 &&
+                        (curd[p] < 0 || curd[p] > entry_start(cur[p]) || curd[p] >= pv.max_position))
+                        n[p] = -1;
                     live = live || (n[p] > 0 && entry_start(cur[p]) <= m_hi);
                 }
                 if (j == T || live) {
@@ -286,14 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int p = 0; p < kPagesPerTile; ++p) {
                         tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
                         tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
-                        const float2* base = pv.rope + (n[p] > 0 ? (size_t)entry_start(cur[p]) * (kD / 2) : 0);
+                        const int rowpos = LOCAL ? curd[p] : entry_start(cur[p]);   // position of the page's rotation
+                        const float2* base = pv.rope + (n[p] > 0 ? (size_t)rowpos * (kD / 2) : 0);
                         bulk_load(bs + p * 512, base, 512, fb);
                     }
                     last_k[st] = k;
                     ++k;
                 }
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) cur[p] = nxt[p];
+                for (int p = 0; p < kPagesPerTile; ++p) {
+                    cur[p] = nxt[p];
+                    curd[p] = nxtd[p];
+                }
             }
             if (!ok) *abort_flag = 1;
             if (*abort_flag) {   // let issued copies land before the CTA's smem is released
@@ -479,7 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int w = 0; w < 2; ++w) {
                                 const int f = 2 * v + w;
                                 const float cb = w ? b.z : b.x, sb = w ? b.w : b.y;
-                                const float c = cb * cs[f] - sb * sn[f], s = sb * cs[f] + cb * sn[f];
+                                // LOCAL: the page's one relative rotation; else start + slot
+                                const float c = LOCAL ? cb : cb * cs[f] - sb * sn[f];
+                                const float s = LOCAL ? sb : sb * cs[f] + cb * sn[f];
                                 const float a = x1[f], z = x2[f];
                                 x1[f] = a * c - z * s;
                                 x2[f] = a * s + z * c;
@@ -699,10 +714,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int prefill_init() {
-    if (cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(prefill_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(prefill_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(prefill_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
         return LAZYATTN_ECUDA;
     return LAZYATTN_OK;
 }
@@ -724,9 +741,12 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     P.total_q = b.total_q;
     P.g = g;
     P.oob_row = (int32_t)rows;
+    P.entry_delta = b.entry_delta;
     const int TQ = kRows / g;
     dim3 grid((b.max_q_len + TQ - 1) / TQ, p.d.n_kv_heads, b.num_requests);
-    auto kern = (b.flags & LAZYATTN_KEYS_PREROTATED) ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    auto kern = p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL
+                    ? prefill_tc_kernel<false, true>
+                    : ((b.flags & LAZYATTN_KEYS_PREROTATED) ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }

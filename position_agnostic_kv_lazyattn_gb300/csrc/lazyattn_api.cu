@@ -110,6 +110,9 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         return LAZYATTN_EINVAL;
     if (!d.k_pool || !d.v_pool || !d.rope_table || !d.status_word) return LAZYATTN_EINVAL;
     if (d.rope_scaling < LAZYATTN_ROPE_DEFAULT || d.rope_scaling > LAZYATTN_ROPE_LLAMA3) return LAZYATTN_EINVAL;
+    if (d.key_storage != LAZYATTN_KEYS_POSITION_FREE &&
+        !(d.key_storage == LAZYATTN_KEYS_DOC_LOCAL && d.dtype == LAZYATTN_BF16))
+        return LAZYATTN_EINVAL;
     if (d.rope_scaling != LAZYATTN_ROPE_DEFAULT && !(d.rope_factor >= 1.0)) return LAZYATTN_EINVAL;
     if ((d.rope_scaling == LAZYATTN_ROPE_YARN || d.rope_scaling == LAZYATTN_ROPE_LLAMA3) &&
         (d.rope_original_max_position < 1 || !(d.rope_low >= 0.0) || !(d.rope_high > d.rope_low)))
@@ -224,6 +227,7 @@ int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32
     if (!aligned16(k) || !aligned16(v)) return LAZYATTN_EINVAL;
     const int32_t np = (n_tokens + kPage - 1) / kPage;
     if (out_cap < np) return LAZYATTN_EINVAL;
+    if (pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL && n_tokens > pool->d.max_position) return LAZYATTN_EINVAL;
     int rc = lazyattn_alloc_pages(pool, np, out_pages);
     if (rc != LAZYATTN_OK) return rc;
     rc = launch_store_pages(*pool, k, v, n_tokens, out_pages, np, static_cast<cudaStream_t>(stream));
@@ -239,6 +243,9 @@ static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int o
     if (!pool || !b) return LAZYATTN_EINVAL;
     if (b->num_requests < 1 || b->max_entries < 0 || !b->entries || !b->entry_offsets) return LAZYATTN_EINVAL;
     if (b->flags & ~LAZYATTN_KEYS_PREROTATED) return LAZYATTN_EINVAL;
+    if (pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL &&
+        ((b->flags & LAZYATTN_KEYS_PREROTATED) || (b->max_entries > 0 && !b->entry_delta)))
+        return LAZYATTN_EINVAL;
     if (op == LAZYATTN_OP_PREFILL) {
         if (b->total_q < 0 || b->max_q_len < 0 || !b->q_offsets || !b->q_start) return LAZYATTN_EINVAL;
     }
@@ -298,7 +305,9 @@ int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch, cons
                          void* stream) {
     int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
     if (rc != LAZYATTN_OK) return rc;
-    if (!dst_entries || (batch->flags & LAZYATTN_KEYS_PREROTATED)) return LAZYATTN_EINVAL;
+    if (!dst_entries || (batch->flags & LAZYATTN_KEYS_PREROTATED) ||
+        pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL)
+        return LAZYATTN_EINVAL;
     if (batch->max_entries == 0) return LAZYATTN_OK;
     return launch_materialize(*pool, *batch, dst_entries, static_cast<cudaStream_t>(stream));
 }

@@ -25,6 +25,8 @@ LAZYATTN_ROPE_LINEAR = 1
 LAZYATTN_ROPE_NTK = 2
 LAZYATTN_ROPE_YARN = 3
 LAZYATTN_ROPE_LLAMA3 = 4
+LAZYATTN_KEYS_POSITION_FREE = 0
+LAZYATTN_KEYS_DOC_LOCAL = 1
 
 STATUS = {
     0: "LAZYATTN_OK", -1: "LAZYATTN_EINVAL", -2: "LAZYATTN_ENOSPC", -3: "LAZYATTN_ERANGE",
@@ -48,6 +50,7 @@ class lazyattn_pool_desc(ctypes.Structure):
         ("status_word", ctypes.c_void_p),
         ("rope_scaling", ctypes.c_int32), ("rope_original_max_position", ctypes.c_int32),
         ("rope_factor", ctypes.c_double), ("rope_low", ctypes.c_double), ("rope_high", ctypes.c_double),
+        ("key_storage", ctypes.c_int32),
     ]
 
 
@@ -56,6 +59,7 @@ class lazyattn_batch(ctypes.Structure):
         ("num_requests", ctypes.c_int32), ("max_entries", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("total_q", ctypes.c_int32), ("entries", ctypes.c_void_p), ("entry_offsets", ctypes.c_void_p),
         ("q_offsets", ctypes.c_void_p), ("q_start", ctypes.c_void_p), ("flags", ctypes.c_int32),
+        ("entry_delta", ctypes.c_void_p),
     ]
 
 
@@ -175,10 +179,10 @@ def lazyattn_store_doc(pool: int, k, v, n_tokens: int, stream=None):
 # --------------------------------------------------------------------- batches
 
 def make_batch(num_requests, max_entries, entries, entry_offsets, q_offsets=None, q_start=None,
-               max_q_len=0, total_q=0, flags=0) -> lazyattn_batch:
-    """Fill a lazyattn_batch from device tensors (int64 entries, int32 offsets)."""
+               max_q_len=0, total_q=0, flags=0, entry_delta=None) -> lazyattn_batch:
+    """Fill a lazyattn_batch from device tensors (int64 entries, int32 offsets and deltas)."""
     return lazyattn_batch(num_requests, max_entries, max_q_len, total_q, _ptr(entries), _ptr(entry_offsets),
-                          _ptr(q_offsets), _ptr(q_start), flags)
+                          _ptr(q_offsets), _ptr(q_start), flags, _ptr(entry_delta))
 
 
 def lazyattn_workspace_size(pool: int, op: int, batch: lazyattn_batch) -> int:

@@ -30,19 +30,25 @@ def pack_entries(pages, starts, nvalid, writable) -> np.ndarray:
 @dataclasses.dataclass
 class Segment:
     """A run of tokens stored in consecutive entries: page ids, logical start,
-    token count, and whether decode may append into its pages."""
+    token count, whether decode may append into its pages, and (doc-local
+    pools) the logical position of the run's local position 0, by default its
+    start: a run stored by one lazyattn_store_doc call."""
     pages: Sequence[int]
     start: int
     n_tokens: int
     writable: bool = False
+    delta: int = None
 
 
 class DevicePool:
     def __init__(self, num_pages: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: str,
-                 rope_theta: float, max_position: int, device="cuda", stream=None, rope_scaling=None):
+                 rope_theta: float, max_position: int, device="cuda", stream=None, rope_scaling=None,
+                 key_storage: str = "position_free"):
         """rope_scaling: None (plain RoPE) or a dict with "kind" in {"linear", "ntk",
         "yarn", "llama3"}, "factor" and, for yarn / llama3, "original_max_position",
-        "low", "high" (see lazyattn.h)."""
+        "low", "high" (see lazyattn.h). key_storage: "position_free" (keys stored
+        without RoPE) or "doc_local" (the paper's layout: keys stored rotated at
+        document-local positions; bf16 only)."""
         self.dtype = dtype
         self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
@@ -67,6 +73,9 @@ class DevicePool:
             self.desc.rope_original_max_position = int(rope_scaling.get("original_max_position", 0))
             self.desc.rope_low = float(rope_scaling.get("low", 0.0))
             self.desc.rope_high = float(rope_scaling.get("high", 0.0))
+        self.key_storage = key_storage
+        self.desc.key_storage = {"position_free": L.LAZYATTN_KEYS_POSITION_FREE,
+                                 "doc_local": L.LAZYATTN_KEYS_DOC_LOCAL}[key_storage]
         self.handle = L.lazyattn_pool_create(self.desc, stream)
 
     def close(self):
@@ -110,11 +119,12 @@ class Batch:
 
     def __init__(self, requests: Sequence[Sequence[Segment]], q_lens: Sequence[int] = (),
                  q_starts: Sequence[int] = (), device="cuda", flags: int = 0):
-        pg, st, nv, wr, offs = [], [], [], [], [0]
+        pg, st, nv, wr, dl, offs = [], [], [], [], [], [0]
         for segs in requests:
             for seg in segs:
                 a, b, c, d = segment_entries(seg)
                 pg += a; st += b; nv += c; wr += d
+                dl += [seg.start if seg.delta is None else seg.delta] * len(a)
             offs.append(len(pg))
         self.entries_host = pack_entries(pg, st, nv, wr) if pg else np.zeros(0, np.uint64)
         self.offsets_host = np.array(offs, np.int32)
@@ -124,6 +134,8 @@ class Batch:
         if self.entries.numel() == 0:
             self.entries = torch.zeros(1, dtype=torch.int64, device=device)
         self.entry_offsets = torch.from_numpy(self.offsets_host).to(device)
+        self.delta_host = np.array(dl if dl else [0], np.int32)
+        self.entry_delta = torch.from_numpy(self.delta_host).to(device)
         q_lens = list(q_lens)
         if q_lens:
             qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
@@ -136,7 +148,7 @@ class Batch:
             self.total_q = self.max_q_len = 0
         self.flags = flags
         self.c = L.make_batch(self.num_requests, self.max_entries, self.entries, self.entry_offsets,
-                              self.q_offsets, self.q_start, self.max_q_len, self.total_q, flags)
+                              self.q_offsets, self.q_start, self.max_q_len, self.total_q, flags, self.entry_delta)
 
     def with_entries(self, entries_host: np.ndarray, flags: int, device="cuda") -> "Batch":
         """Same requests and query layout, another entry array (e.g. materialised pages)."""
@@ -146,5 +158,5 @@ class Batch:
         b.entries = torch.from_numpy(b.entries_host.view(np.int64).copy()).to(device)
         b.flags = flags
         b.c = L.make_batch(b.num_requests, b.max_entries, b.entries, b.entry_offsets, b.q_offsets, b.q_start,
-                           b.max_q_len, b.total_q, flags)
+                           b.max_q_len, b.total_q, flags, b.entry_delta)
         return b
