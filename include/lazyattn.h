@@ -93,6 +93,12 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
  *                 stores K rotated at document-local positions (token i of the call at i),
  *                 prefill applies one relative rotation by the document's offset, decode
  *                 rotates q instead of the keys; batches must then carry entry_delta.
+ *   rope_interleaved  0: rotate-half pairs (i, i + D/2); 1 (bf16 pools only): interleaved pairs
+ *                 (2i, 2i+1) with the same frequencies, as in the original RoPE / Llama layout.
+ *                 q and k are then given and stored in their natural order; the library
+ *                 de-interleaves them where they enter (store, append, q loads): a score is a
+ *                 dot product over the head dimension, so one permutation applied to both q
+ *                 and k leaves it unchanged, and v is never permuted.
  * A zero-initialised descriptor tail means plain RoPE and position-free keys.
  */
 typedef struct lazyattn_pool_desc {
@@ -114,6 +120,7 @@ typedef struct lazyattn_pool_desc {
     double rope_low;
     double rope_high;
     int32_t key_storage;
+    int32_t rope_interleaved;
 } lazyattn_pool_desc;
 
 #define LAZYATTN_KEYS_POSITION_FREE 0

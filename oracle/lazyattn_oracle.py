@@ -101,9 +101,13 @@ class RopeSpec:
     """
 
     def __init__(self, base: float, kind: str = "default", factor: float = 1.0,
-                 original_max_position: int = 0, low: float = 0.0, high: float = 0.0):
+                 original_max_position: int = 0, low: float = 0.0, high: float = 0.0, pairing: str = "half"):
+        """pairing: "half" rotates (x[i], x[i + D/2]) (the paper's half-dimensions);
+        "interleaved" rotates (x[2i], x[2i+1]) (RoFormer's original form, Llama's
+        layout), with the same frequencies theta_i."""
         self.base, self.kind, self.factor = float(base), kind, float(factor)
         self.original, self.low, self.high = float(original_max_position), float(low), float(high)
+        self.pairing = pairing
 
     def inv_freq(self, head_dim: int) -> np.ndarray:
         i = np.arange(head_dim // 2, dtype=np.float64)
@@ -159,6 +163,12 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     D = x.shape[-1]
     ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(D, theta)
     c, s = np.cos(ang), np.sin(ang)
+    if isinstance(theta, RopeSpec) and theta.pairing == "interleaved":
+        x1, x2 = x[..., 0::2], x[..., 1::2]
+        out = np.empty(np.broadcast_shapes(x.shape, c.shape[:-1] + (D,)), dtype=np.float64)
+        out[..., 0::2] = x1 * c - x2 * s
+        out[..., 1::2] = x1 * s + x2 * c
+        return out
     x1, x2 = x[..., : D // 2], x[..., D // 2:]
     return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
 

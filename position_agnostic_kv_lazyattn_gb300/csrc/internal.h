@@ -63,7 +63,21 @@ struct PoolView {
     int32_t max_position;
     int32_t hq, hkv, d;
     float qk_scale;       // logit scale: 1/sqrt(D), times YaRN's attention temperature
+    int32_t interleaved;  // q/k arrive with interleaved RoPE pairs (2i, 2i+1): de-interleave on load
 };
+
+// Interleaved RoPE pairs: from 16 consecutive bf16 of a q or k row (two uint4,
+// elements 16u .. 16u+15), the 8 even elements (pair members 2i, which become
+// dims 8u.. of the first half) and the 8 odd ones (dims 64+8u.. of the second).
+// (Safe when even / odd alias a / b: both results are formed before either is written.)
+__device__ __forceinline__ void deinterleave16(const uint4& a, const uint4& b, uint4& even, uint4& odd) {
+    const uint4 e = make_uint4(__byte_perm(a.x, a.y, 0x5410), __byte_perm(a.z, a.w, 0x5410),
+                               __byte_perm(b.x, b.y, 0x5410), __byte_perm(b.z, b.w, 0x5410));
+    const uint4 o = make_uint4(__byte_perm(a.x, a.y, 0x7632), __byte_perm(a.z, a.w, 0x7632),
+                               __byte_perm(b.x, b.y, 0x7632), __byte_perm(b.z, b.w, 0x7632));
+    even = e;
+    odd = o;
+}
 
 // Record the first device-side error; later ones are dropped.
 __device__ __forceinline__ void record_error(int32_t* status, int32_t code) {

@@ -278,8 +278,15 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int d = 16 * t + 2 * c + 8 * hf;
-                qx[t][hf] = gr < g ? __ldg(qp + d / 2) : 0u;
-                qy[t][hf] = gr < g ? __ldg(qp + (d + 64) / 2) : 0u;
+                uint32_t x = gr < g ? __ldg(qp + (pv.interleaved ? d : d / 2)) : 0u;
+                uint32_t y = gr < g ? __ldg(qp + (pv.interleaved ? d + 1 : (d + 64) / 2)) : 0u;
+                if (pv.interleaved) {   // (2d, 2d+1), (2d+2, 2d+3) -> dims (d, d+1) and (d+64, d+65)
+                    const uint32_t p0 = x, p1 = y;
+                    x = __byte_perm(p0, p1, 0x5410);
+                    y = __byte_perm(p0, p1, 0x7632);
+                }
+                qx[t][hf] = x;
+                qy[t][hf] = y;
             }
 #pragma unroll
         for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
@@ -292,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int d = 16 * t + 2 * c + 8 * hf;
-                const uint32_t x = __ldg(qp + d / 2), y = __ldg(qp + (d + 64) / 2);
+                uint32_t x = __ldg(qp + (pv.interleaved ? d : d / 2)), y = __ldg(qp + (pv.interleaved ? d + 1 : (d + 64) / 2));
+                if (pv.interleaved) {   // (2d, 2d+1), (2d+2, 2d+3) -> dims (d, d+1) and (d+64, d+65)
+                    const uint32_t p0 = x, p1 = y;
+                    x = __byte_perm(p0, p1, 0x5410);
+                    y = __byte_perm(p0, p1, 0x7632);
+                }
                 const float4 cs = __ldg(row + d / 2);
                 const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
                 qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);

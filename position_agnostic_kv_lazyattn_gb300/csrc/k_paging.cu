@@ -28,14 +28,36 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 
 // src [n_tokens][Hkv][D] -> pages [page][Hkv][16][D]; one block per (page, kv head).
 // Slots past n_tokens in the last page are zero-filled.
+// interleaved (bf16): K rows are de-interleaved on the way (pairs (2i, 2i+1) of
+// an interleaved-RoPE model become the rotate-half pairs (i, i + D/2)).
 __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* kp, uint4* vp,
                                    int32_t n_tokens, int32_t first_page_index, PageList pages, int hkv,
-                                   int row_vecs) {
+                                   int row_vecs, int interleaved) {
     const int j = blockIdx.x;          // page index within this launch
     const int h = blockIdx.y;
     const int32_t page = pages.ids[j];
     const int tok0 = (first_page_index + j) * kPage;
     const size_t dst_base = ((size_t)page * hkv + h) * kPage * row_vecs;
+    if (interleaved) {
+        const int hv = row_vecs / 2;
+        for (int i = threadIdx.x; i < kPage * hv; i += blockDim.x) {
+            const int slot = i / hv, u = i % hv;
+            const int tok = tok0 + slot;
+            uint4 ev = make_uint4(0, 0, 0, 0), od = ev;
+            if (tok < n_tokens) {
+                const size_t src = ((size_t)tok * hkv + h) * row_vecs + 2 * u;
+                deinterleave16(k[src], k[src + 1], ev, od);
+            }
+            kp[dst_base + (size_t)slot * row_vecs + u] = ev;
+            kp[dst_base + (size_t)slot * row_vecs + hv + u] = od;
+        }
+        for (int i = threadIdx.x; i < kPage * row_vecs; i += blockDim.x) {
+            const int slot = i / row_vecs, c = i % row_vecs;
+            const int tok = tok0 + slot;
+            vp[dst_base + i] = tok < n_tokens ? v[((size_t)tok * hkv + h) * row_vecs + c] : make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
     for (int i = threadIdx.x; i < kPage * row_vecs; i += blockDim.x) {
         const int slot = i / row_vecs, c = i % row_vecs;
         const int tok = tok0 + slot;
@@ -56,7 +78,7 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
 // first half) and their rotate-half partners.
 __global__ void store_pages_local_kernel(const __nv_bfloat16* __restrict__ k, const uint4* __restrict__ v,
                                          __nv_bfloat16* kp, uint4* vp, const float2* rope, int32_t n_tokens,
-                                         int32_t first_page_index, PageList pages, int hkv, int D) {
+                                         int32_t first_page_index, PageList pages, int hkv, int D, int interleaved) {
     const int j = blockIdx.x, h = blockIdx.y;
     const int32_t page = pages.ids[j];
     const int tok0 = (first_page_index + j) * kPage;
@@ -70,8 +92,16 @@ __global__ void store_pages_local_kernel(const __nv_bfloat16* __restrict__ k, co
         if (tok < n_tokens) {
             const __nv_bfloat16* src = k + ((size_t)tok * hkv + h) * D;
             __nv_bfloat16 x[8], y[8];
-            *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(src + d);
-            *reinterpret_cast<uint4*>(y) = *reinterpret_cast<const uint4*>(src + d + half);
+            if (interleaved) {
+                uint4 ev, od;
+                deinterleave16(*reinterpret_cast<const uint4*>(src + 2 * d), *reinterpret_cast<const uint4*>(src + 2 * d + 8),
+                               ev, od);
+                *reinterpret_cast<uint4*>(x) = ev;
+                *reinterpret_cast<uint4*>(y) = od;
+            } else {
+                *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(src + d);
+                *reinterpret_cast<uint4*>(y) = *reinterpret_cast<const uint4*>(src + d + half);
+            }
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const float2 cs = rope[(size_t)tok * half + d + t];
@@ -175,8 +205,14 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
             const int h = i / g8, d = (i % g8) * 8;
             const size_t src = ((size_t)r * pv.hkv + h) * D;
             const size_t dst = (((size_t)page * pv.hkv + h) * kPage + slot) * D;
-            uint4 k1 = *reinterpret_cast<const uint4*>(k_new + src + d);
-            uint4 k2 = *reinterpret_cast<const uint4*>(k_new + src + d + half);
+            uint4 k1, k2;
+            if (pv.interleaved) {
+                deinterleave16(*reinterpret_cast<const uint4*>(k_new + src + 2 * d),
+                               *reinterpret_cast<const uint4*>(k_new + src + 2 * d + 8), k1, k2);
+            } else {
+                k1 = *reinterpret_cast<const uint4*>(k_new + src + d);
+                k2 = *reinterpret_cast<const uint4*>(k_new + src + d + half);
+            }
             const uint4 v1 = *reinterpret_cast<const uint4*>(v_new + src + d);
             const uint4 v2 = *reinterpret_cast<const uint4*>(v_new + src + d + half);
             if (PREROT) {
@@ -318,11 +354,13 @@ int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int
             store_pages_local_kernel<<<grid, 128, 0, stream>>>(
                 static_cast<const __nv_bfloat16*>(k), static_cast<const uint4*>(v),
                 static_cast<__nv_bfloat16*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
-                static_cast<const float2*>(p.d.rope_table), n_tokens, first, pl, p.d.n_kv_heads, p.d.head_dim);
+                static_cast<const float2*>(p.d.rope_table), n_tokens, first, pl, p.d.n_kv_heads, p.d.head_dim,
+                p.d.rope_interleaved);
         else
             store_pages_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                                                          static_cast<uint4*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
-                                                         n_tokens, first, pl, p.d.n_kv_heads, row_vecs);
+                                                         n_tokens, first, pl, p.d.n_kv_heads, row_vecs,
+                                                         p.d.rope_interleaved);
         if (cuda_status() != LAZYATTN_OK) return LAZYATTN_ECUDA;
     }
     return LAZYATTN_OK;

@@ -157,7 +157,8 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 // PREROT: keys already rotated at their logical positions (no rotation).
 // LOCAL: keys rotated at document-local positions; each page takes one relative
 // rotation by its document's offset (§3.2 "Prefilling": R_delta R_t = R_(delta+t)).
-template <bool PREROT, bool LOCAL>
+// INTER: q arrives with interleaved RoPE pairs and is de-interleaved on load.
+template <bool PREROT, bool LOCAL, bool INTER>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, PoolView pv,
                       PrefillParams P) {
@@ -552,8 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 w1 = make_uint4(0, 0, 0, 0), w2 = w1;
                 if (row_valid) {
                     float x1[8], x2[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(qp_ + 8 * u)), x1);
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(qp_ + 64 + 8 * u)), x2);
+                    uint4 a = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u : 8 * u)));
+                    uint4 b = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u + 8 : 64 + 8 * u)));
+                    if (INTER) deinterleave16(a, b, a, b);
+                    unpack8(a, x1);
+                    unpack8(b, x2);
                     const float4* c4 = reinterpret_cast<const float4*>(cs + 16 * u);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -713,14 +717,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, PoolView, PrefillParams);
+
+// The instantiation for a pool and a batch: key layout and pairing of the pool,
+// pre-rotated pages of the batch.
+PrefillKernel prefill_kernel_for(bool prerot, bool local, bool inter) {
+    if (local) return inter ? prefill_tc_kernel<false, true, true> : prefill_tc_kernel<false, true, false>;
+    if (prerot) return inter ? prefill_tc_kernel<true, false, true> : prefill_tc_kernel<true, false, false>;
+    return inter ? prefill_tc_kernel<false, false, true> : prefill_tc_kernel<false, false, false>;
+}
+
 int prefill_init() {
-    if (cudaFuncSetAttribute(prefill_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(prefill_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(prefill_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-        return LAZYATTN_ECUDA;
+    for (int i = 0; i < 8; ++i) {
+        if ((i & 1) && (i & 2)) continue;   // pre-rotated pages are never doc-local
+        if (cudaFuncSetAttribute(prefill_kernel_for(i & 1, i & 2, i & 4), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return LAZYATTN_ECUDA;
+    }
     return LAZYATTN_OK;
 }
 
@@ -744,9 +757,8 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     P.entry_delta = b.entry_delta;
     const int TQ = kRows / g;
     dim3 grid((b.max_q_len + TQ - 1) / TQ, p.d.n_kv_heads, b.num_requests);
-    auto kern = p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL
-                    ? prefill_tc_kernel<false, true>
-                    : ((b.flags & LAZYATTN_KEYS_PREROTATED) ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>);
+    auto kern = prefill_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0,
+                                   p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }

@@ -23,6 +23,7 @@ lazyattn::PoolView lazyattn_pool::view() const {
     v.hkv = d.n_kv_heads;
     v.d = d.head_dim;
     v.qk_scale = qk_scale;
+    v.interleaved = d.rope_interleaved;
     return v;
 }
 
@@ -110,6 +111,7 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         return LAZYATTN_EINVAL;
     if (!d.k_pool || !d.v_pool || !d.rope_table || !d.status_word) return LAZYATTN_EINVAL;
     if (d.rope_scaling < LAZYATTN_ROPE_DEFAULT || d.rope_scaling > LAZYATTN_ROPE_LLAMA3) return LAZYATTN_EINVAL;
+    if (d.rope_interleaved != 0 && !(d.rope_interleaved == 1 && d.dtype == LAZYATTN_BF16)) return LAZYATTN_EINVAL;
     if (d.key_storage != LAZYATTN_KEYS_POSITION_FREE &&
         !(d.key_storage == LAZYATTN_KEYS_DOC_LOCAL && d.dtype == LAZYATTN_BF16))
         return LAZYATTN_EINVAL;

@@ -50,7 +50,7 @@ class lazyattn_pool_desc(ctypes.Structure):
         ("status_word", ctypes.c_void_p),
         ("rope_scaling", ctypes.c_int32), ("rope_original_max_position", ctypes.c_int32),
         ("rope_factor", ctypes.c_double), ("rope_low", ctypes.c_double), ("rope_high", ctypes.c_double),
-        ("key_storage", ctypes.c_int32),
+        ("key_storage", ctypes.c_int32), ("rope_interleaved", ctypes.c_int32),
     ]
 
 

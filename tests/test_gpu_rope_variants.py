@@ -2,7 +2,7 @@
 / NTK and YaRN keep the score form; the kernels take the variant's position
 table and logit scale) against the fp64 oracle's own restatement of each
 variant: prefill of two requests that share a document at different offsets,
-then two decode steps, for bf16 and for the fp32 path.
+then two decode steps, for bf16 (both key layouts) and for the fp32 path.
 """
 import numpy as np
 import pytest
@@ -21,6 +21,9 @@ VARIANTS = {
     "ntk": dict(kind="ntk", factor=8.0),
     "yarn": dict(kind="yarn", factor=8.0, original_max_position=256, low=1.0, high=32.0),
     "llama3": dict(kind="llama3", factor=8.0, original_max_position=512, low=1.0, high=4.0),
+    "interleaved": dict(kind="default", factor=1.0, interleaved=True),
+    "yarn+interleaved": dict(kind="yarn", factor=8.0, original_max_position=256, low=1.0, high=32.0,
+                             interleaved=True),
 }
 
 
@@ -36,15 +39,18 @@ def L():
 
 def _spec(cfg, v):
     return RopeSpec(cfg.rope_theta, v["kind"], v["factor"], v.get("original_max_position", 0), v.get("low", 0.0),
-                    v.get("high", 0.0))
+                    v.get("high", 0.0), "interleaved" if v.get("interleaved") else "half")
 
 
-@pytest.mark.parametrize("config", ["llama3_8b", "tiny_fp32"])
+@pytest.mark.parametrize("config,keys", [("llama3_8b", "position_free"), ("llama3_8b", "doc_local"),
+                                         ("tiny_fp32", "position_free")])
 @pytest.mark.parametrize("variant", list(VARIANTS))
-def test_rope_variant_prefill_and_decode(L, config, variant):
+def test_rope_variant_prefill_and_decode(L, config, keys, variant):
     from position_agnostic_kv_lazyattn_gb300 import Batch, DevicePool, Segment
     cfg = workload.CONFIGS[config]
     v = VARIANTS[variant]
+    if v.get("interleaved") and cfg.dtype != "bf16":
+        pytest.skip("interleaved pairing is supported for bf16 pools")
     spec = _spec(cfg, v)
     rng = np.random.default_rng(11)
     plan = [([1, 2, 1], 21), ([2, 3], 21)]   # document 1 twice in one request; document 2 at two offsets
@@ -52,8 +58,9 @@ def test_rope_variant_prefill_and_decode(L, config, variant):
     used = sorted({d for docs, _ in plan for d in docs})
     n_pages = len(used) * cfg.doc_pages + len(plan) * (-(-(ql + steps) // 16) + 1) + 4
     max_pos = max(len(docs) for docs, _ in plan) * cfg.doc_len + ql + steps + 16
+    scaling = None if v["kind"] == "default" else {x: y for x, y in v.items() if x != "interleaved"}
     pool = DevicePool(n_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta, max_pos,
-                      rope_scaling=v)
+                      rope_scaling=scaling, rope_interleaved=bool(v.get("interleaved")), key_storage=keys)
     dev = lambda a: workload.device.to_device(a, cfg.dtype)   # noqa: E731
     rnd = lambda shape: workload.round_bf16(rng.standard_normal(shape).astype(np.float32)) \
         if cfg.dtype == "bf16" else rng.standard_normal(shape).astype(np.float32)   # noqa: E731

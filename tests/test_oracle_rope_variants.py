@@ -92,3 +92,32 @@ def test_yarn_temperature_enters_the_logits():
     p = np.exp(logits - logits.max())
     want = (p / p.sum()) @ v[:, 0, :]
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_interleaved_pairing_complex_form():
+    """Interleaved pairs (x[2i], x[2i+1]) rotate as the complex numbers
+    x[2i] + i x[2i+1] multiplied by exp(i p theta_i) (RoFormer's form)."""
+    rng = np.random.default_rng(3)
+    for Dm in (8, 64, 128):
+        x = rng.standard_normal(Dm)
+        for pos in (0, 3, 777, 30000):
+            spec = RopeSpec(1e4, pairing="interleaved")
+            got = oracle.rope(x, pos, spec)
+            z = (x[0::2] + 1j * x[1::2]) * np.exp(1j * pos * np.power(1e4, -2.0 * np.arange(Dm // 2) / Dm))
+            want = np.empty(Dm)
+            want[0::2], want[1::2] = z.real, z.imag
+            np.testing.assert_allclose(got, want, rtol=0, atol=1e-10)
+
+
+def test_interleaved_scores_equal_half_pairing_on_permuted_vectors():
+    """A score is a dot product over the head dimension, so interleaved RoPE on
+    (q, k) equals rotate-half RoPE on both vectors with evens moved to the first
+    half and odds to the second (the layout the library stores)."""
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])
+    inter = RopeSpec(BASE, pairing="interleaved")
+    for m, n in ((0, 0), (5, 2), (4000, 17), (33000, 32999)):
+        a = oracle.rope(q, m, inter) @ oracle.rope(k, n, inter)
+        b = oracle.rope(q[perm], m, BASE) @ oracle.rope(k[perm], n, BASE)
+        assert a == pytest.approx(b, rel=1e-12, abs=1e-12)
