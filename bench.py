@@ -149,8 +149,9 @@ def run_ours(args, rank, world):
     if args.requests:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_requests=min(args.requests, cfg.n_requests))
-    doc_local = args.keys == "doc_local"
-    env = wdev.setup(cfg, baseline=not args.no_extras and not doc_local, key_storage=args.keys)
+    doc_local = args.keys == "doc_local" or args.pos == "alibi"   # no materialising baseline / no-RoPE leg
+    env = wdev.setup(cfg, baseline=not args.no_extras and not doc_local, key_storage=args.keys,
+                     position_encoding=args.pos)
     R = cfg.n_requests
     b = env.batch
     stream = torch.cuda.current_stream()
@@ -380,7 +381,7 @@ def run_ours(args, rank, world):
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "query_len": cfg.q_len,
                    "decode_steps": cfg.decode_steps, "zipf_alpha": cfg.zipf_alpha, "seed": cfg.seed,
                    "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
-                   "keys": args.keys},
+                   "keys": args.keys, "position_encoding": args.pos},
         "prefill_tflops": round(pre_tflops, 2), "ttft_ms": round(local["pre_ms"], 4),
         "decode_ms_per_token_step": round(mean_call, 4),
         "median_step_ms": round(statistics.median(step_ms), 4),
@@ -498,6 +499,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--keys", default="position_free", choices=["position_free", "doc_local"],
                     help="key layout: stored without RoPE (default) or rotated at document-local positions")
+    ap.add_argument("--pos", default="rope", choices=["rope", "alibi"],
+                    help="position encoding: RoPE (default) or the ALiBi score bias")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

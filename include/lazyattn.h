@@ -99,6 +99,12 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
  *                 de-interleaves them where they enter (store, append, q loads): a score is a
  *                 dot product over the head dimension, so one permutation applied to both q
  *                 and k leaves it unchanged, and v is never permuted.
+ *   position_encoding  LAZYATTN_POS_ROPE (0) or LAZYATTN_POS_ALIBI (bf16 pools; §3.5 "Score-space
+ *                 positional methods"): no rotation at all; every score q.k / sqrt(D) gets the
+ *                 bias -slope_h * (m - n) for query head h at position m and key position n,
+ *                 with the ALiBi slopes of Hq heads (2^(-8 (h+1) / Hq) for a power of two;
+ *                 otherwise those of the power of two below Hq, then every other slope of
+ *                 twice that). Requires plain RoPE fields, position-free keys, no interleaving.
  * A zero-initialised descriptor tail means plain RoPE and position-free keys.
  */
 typedef struct lazyattn_pool_desc {
@@ -121,7 +127,11 @@ typedef struct lazyattn_pool_desc {
     double rope_high;
     int32_t key_storage;
     int32_t rope_interleaved;
+    int32_t position_encoding;
 } lazyattn_pool_desc;
+
+#define LAZYATTN_POS_ROPE 0
+#define LAZYATTN_POS_ALIBI 1
 
 #define LAZYATTN_KEYS_POSITION_FREE 0
 #define LAZYATTN_KEYS_DOC_LOCAL 1

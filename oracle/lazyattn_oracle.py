@@ -40,7 +40,8 @@ from typing import Iterable, List, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "PAGE_SIZE", "unpack_entry", "resolve_entries", "RopeSpec", "rope_inv_freq", "logit_scale", "rope",
+    "PAGE_SIZE", "unpack_entry", "resolve_entries", "RopeSpec", "AlibiSpec", "alibi_slopes", "rope_inv_freq",
+    "logit_scale", "rope",
     "attention", "prefill_request", "decode_request", "materialize_rotated",
     "attention_prerotated", "paged_context", "paged_prefill", "paged_decode_step",
 ]
@@ -138,6 +139,29 @@ class RopeSpec:
         return float(scale)
 
 
+class AlibiSpec:
+    """ALiBi instead of RoPE (§3.5, "Score-space positional methods": the bias
+    is added to the score rather than rotating q and k, so it too can be
+    applied lazily from logical positions). Passed where the other functions
+    take the RoPE base: q and k are not rotated, and the score of query head h
+    at position m with a key at position n gets -slope_h * (m - n)."""
+
+
+def alibi_slopes(n_heads: int) -> np.ndarray:
+    """ALiBi head slopes (Press et al.): for n a power of two, the geometric
+    sequence 2^(-8/n), 2^(-16/n), ..., 2^(-8); otherwise the slopes for the
+    largest power of two p below n, followed by the 1st, 3rd, 5th, ... slopes
+    of the sequence for 2p, up to n in all."""
+    def geometric(n):
+        return [2.0 ** (-8.0 * (i + 1) / n) for i in range(n)]
+    p = 1
+    while p * 2 <= n_heads:
+        p *= 2
+    if p == n_heads:
+        return np.array(geometric(n_heads))
+    return np.array(geometric(p) + geometric(2 * p)[0::2][: n_heads - p])
+
+
 def rope_inv_freq(head_dim: int, theta) -> np.ndarray:
     """theta_i, i = 0 .. D/2-1, fp64: base^(-2i/D) for a plain base (a number),
     or the variant's frequencies for a RopeSpec."""
@@ -178,11 +202,13 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def attention_prerotated(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray,
-                         q_pos: np.ndarray, k_pos: np.ndarray, scale: float = None) -> np.ndarray:
+                         q_pos: np.ndarray, k_pos: np.ndarray, scale: float = None,
+                         alibi: np.ndarray = None) -> np.ndarray:
     """Causal softmax attention over already rotated q and k.
 
     q_rot: [Lq][Hq][D]; k_rot, v: [L][Hkv][D]; q_pos: [Lq]; k_pos: [L];
-    scale: logit scale, 1/sqrt(D) when None.
+    scale: logit scale, 1/sqrt(D) when None; alibi: per query head slopes
+    of an ALiBi bias -slope * (q_pos - k_pos), or None.
     Returns [Lq][Hq][D] fp64.
     """
     q_rot = np.asarray(q_rot, np.float64)
@@ -196,6 +222,8 @@ def attention_prerotated(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray,
     for h in range(Hq):
         kv = h // g
         s = (q_rot[:, h, :] @ k_rot[:, kv, :].T) * (1.0 / np.sqrt(np.float64(D)) if scale is None else scale)
+        if alibi is not None:
+            s = s - alibi[h] * (np.asarray(q_pos, np.float64)[:, None] - np.asarray(k_pos, np.float64)[None, :])
         s = np.where(visible, s, -np.inf)
         m = s.max(axis=1, keepdims=True)
         p = np.exp(s - m)
@@ -209,6 +237,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos, k_pos,
     """Lazy form: q and k arrive without positions and are rotated here."""
     q_pos = np.asarray(q_pos, dtype=np.int64)
     k_pos = np.asarray(k_pos, dtype=np.int64)
+    if isinstance(theta, AlibiSpec):
+        return attention_prerotated(q, k, v, q_pos, k_pos, None, alibi_slopes(np.asarray(q).shape[1]))
     q_rot = rope(q, q_pos[:, None], theta)
     k_rot = rope(k, k_pos[:, None], theta)
     return attention_prerotated(q_rot, k_rot, v, q_pos, k_pos, logit_scale(np.asarray(q).shape[-1], theta))

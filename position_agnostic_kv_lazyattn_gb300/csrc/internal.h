@@ -66,6 +66,16 @@ struct PoolView {
     int32_t interleaved;  // q/k arrive with interleaved RoPE pairs (2i, 2i+1): de-interleave on load
 };
 
+// ALiBi slope of query head h out of n (the ALiBi paper's rule): for n a power
+// of two, 2^(-8 (h+1) / n); otherwise the slopes of p = the power of two below
+// n for h < p, then every other slope of 2p (its 1st, 3rd, ...) for h >= p.
+__host__ __device__ inline float alibi_slope(int h, int n) {
+    int p = 1;
+    while (p * 2 <= n) p *= 2;
+    if (h < p) return exp2f(-8.0f * (float)(h + 1) / (float)p);
+    return exp2f(-8.0f * (float)(2 * (h - p) + 1) / (float)(2 * p));
+}
+
 // Interleaved RoPE pairs: from 16 consecutive bf16 of a q or k row (two uint4,
 // elements 16u .. 16u+15), the 8 even elements (pair members 2i, which become
 // dims 8u.. of the first half) and the 8 odd ones (dims 64+8u.. of the second).

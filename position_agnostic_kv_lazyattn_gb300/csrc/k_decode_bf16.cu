@@ -172,11 +172,12 @@ __device__ __forceinline__ int slot_unit(int t, int f4) { return t * (kRowBytes 
 // at document-local positions; instead of the keys, q is rotated at m - delta
 // (its position relative to the page's document), once per change of delta
 // (§3.2 "Decoding": rotate q per document rather than K per token).
-template <bool PREROT, bool LOCAL>
+// ALIBI: no rotation of q or k; each score gets -slope_h (m - n) (§3.5).
+template <bool PREROT, bool LOCAL, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        PoolView pv, DecodeParams P) {
-    constexpr bool ROT_K = !PREROT && !LOCAL;   // keys rotated here
+    constexpr bool ROT_K = !PREROT && !LOCAL && !ALIBI;   // keys rotated here
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_full[kWarps][kStages];
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // the page's row of the position table: its start (ROT_K) or m - delta (LOCAL)
     auto row_of = [&](uint64_t e, int d) {
         const int pos = LOCAL ? m - d : entry_start(e);
-        return (!PREROT && page_n(e, d) > 0)
+        return (!PREROT && !ALIBI && page_n(e, d) > 0)
                    ? __ldg(reinterpret_cast<const float4*>(pv.rope + (size_t)pos * (kD / 2)) + lane)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     };
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     x = __byte_perm(p0, p1, 0x5410);
                     y = __byte_perm(p0, p1, 0x7632);
                 }
-                const float4 cs = __ldg(row + d / 2);
+                const float4 cs = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(row + d / 2);
                 const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
                 qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);
                 qb[t + 4][hf] = pack_h2((a0 * cs.y + b0 * cs.x) * sc, (a1 * cs.w + b1 * cs.z) * sc);
@@ -315,6 +316,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
     }
+
+    // ALiBi slopes of this lane's two heads, in the log2 domain of the scores
+    const float al0 = ALIBI ? alibi_slope(h * g + min(2 * c, g - 1), Hq) * kLog2e : 0.f;
+    const float al1 = ALIBI ? alibi_slope(h * g + min(2 * c + 1, g - 1), Hq) * kLog2e : 0.f;
 
     float o[8][4];
 #pragma unroll
@@ -398,6 +403,13 @@ __global__ void __launch_bounds__(kThreads, 3)
 
             // S^T fragment: (token gr | gr+8) x (head 2c | 2c+1)
             const bool v0 = gr < nv, v1 = gr + 8 < nv;
+            if (ALIBI) {   // tokens start + gr, start + gr + 8; heads 2c, 2c + 1
+                const float dn = (float)(entry_start(e) + gr - m);
+                sacc[0] += al0 * dn;
+                sacc[1] += al1 * dn;
+                sacc[2] += al0 * (dn + 8.f);
+                sacc[3] += al1 * (dn + 8.f);
+            }
             const float s0 = v0 ? sacc[0] : -INFINITY;
             const float s1 = v0 ? sacc[1] : -INFINITY;
             const float s2 = v1 ? sacc[2] : -INFINITY;
@@ -603,14 +615,16 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 int decode_occupancy(int* ctas_per_sm) {
-    if (cudaFuncSetAttribute(decode_bf16_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_bf16_kernel<false, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_bf16_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(decode_bf16_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_bf16_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(decode_bf16_kernel<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_bf16_kernel<false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
         return LAZYATTN_ECUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false, false>, kThreads,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_bf16_kernel<false, false, false>, kThreads,
                                                          kSmemBytes) == cudaSuccess
                ? LAZYATTN_OK
                : LAZYATTN_ECUDA;
@@ -647,9 +661,11 @@ int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __
     P.g = p.d.n_q_heads / p.d.n_kv_heads;
     dim3 grid(L.splits, p.d.n_kv_heads, b.num_requests);
     P.entry_delta = b.entry_delta;
-    auto kern = p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL
-                    ? decode_bf16_kernel<false, true>
-                    : ((b.flags & LAZYATTN_KEYS_PREROTATED) ? decode_bf16_kernel<true, false> : decode_bf16_kernel<false, false>);
+    auto kern = p.d.position_encoding == LAZYATTN_POS_ALIBI ? decode_bf16_kernel<false, false, true>
+                : p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL
+                    ? decode_bf16_kernel<false, true, false>
+                    : ((b.flags & LAZYATTN_KEYS_PREROTATED) ? decode_bf16_kernel<true, false, false>
+                                                             : decode_bf16_kernel<false, false, false>);
     if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.view(), P) != cudaSuccess)
         return LAZYATTN_ECUDA;
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;

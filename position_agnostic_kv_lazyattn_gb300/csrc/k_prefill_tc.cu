@@ -158,7 +158,9 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 // LOCAL: keys rotated at document-local positions; each page takes one relative
 // rotation by its document's offset (§3.2 "Prefilling": R_delta R_t = R_(delta+t)).
 // INTER: q arrives with interleaved RoPE pairs and is de-interleaved on load.
-template <bool PREROT, bool LOCAL, bool INTER>
+// ALIBI: no rotation of q or k; each score gets the bias -slope_h (m - n)
+// (§3.5, score-space positional methods), computed from logical positions.
+template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, PoolView pv,
                       PrefillParams P) {
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float x1[8], x2[8];
                     unpack8(*p1, x1);
                     unpack8(*p2, x2);
-                    if (!PREROT) {
+                    if (!PREROT && !ALIBI) {
                         const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4* c4 = reinterpret_cast<const float4*>(cs + 16 * u);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const float4 f = __ldg(c4 + v);
+                        const float4 f = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(c4 + v);
                         const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
                         x1[2 * v] = (a0 * f.x - z0 * f.y) * sc;
                         x2[2 * v] = (a0 * f.y + z0 * f.x) * sc;
@@ -579,6 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bar_qready));
         }
         const bool active = qi == 0 || tile1;
+        // ALiBi: slope of this row's query head, in the log2 domain of the scores
+        const float alibi_c1 = ALIBI ? alibi_slope(h * g + jh, Hq) * kLog2e : 0.f;
 
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -618,6 +622,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[i] = (m >> (i & 31)) & 1u ? v[i] : 0xff800000u;
                 }
             };
+            // ALiBi bias of key i of half hh (log2 domain; masked keys stay -inf)
+            auto add_bias = [&](uint32_t (&v)[64], int hh) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    // the page's start from the tile info (valid until this warp's P arrival)
+                    const float bp = alibi_c1 * (float)(info.start[4 * hh + q] - m_row);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[16 * q + i] = __float_as_uint(__uint_as_float(v[16 * q + i]) + fmaf(alibi_c1, (float)i, bp));
+                }
+            };
             // pass 1: row maximum over the tile
             float mx8[8];
 #pragma unroll
@@ -627,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
                 if (!wfull) mask64(v, hh);
+                if (ALIBI) add_bias(v, hh);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
@@ -659,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
                 if (!wfull) mask64(v, hh);
+                if (ALIBI) add_bias(v, hh);
                 uint32_t pk[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -721,17 +738,19 @@ using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, PoolView, P
 
 // The instantiation for a pool and a batch: key layout and pairing of the pool,
 // pre-rotated pages of the batch.
-PrefillKernel prefill_kernel_for(bool prerot, bool local, bool inter) {
-    if (local) return inter ? prefill_tc_kernel<false, true, true> : prefill_tc_kernel<false, true, false>;
-    if (prerot) return inter ? prefill_tc_kernel<true, false, true> : prefill_tc_kernel<true, false, false>;
-    return inter ? prefill_tc_kernel<false, false, true> : prefill_tc_kernel<false, false, false>;
+PrefillKernel prefill_kernel_for(bool prerot, bool local, bool inter, bool alibi) {
+    if (alibi) return prefill_tc_kernel<false, false, false, true>;
+    if (local) return inter ? prefill_tc_kernel<false, true, true, false> : prefill_tc_kernel<false, true, false, false>;
+    if (prerot) return inter ? prefill_tc_kernel<true, false, true, false> : prefill_tc_kernel<true, false, false, false>;
+    return inter ? prefill_tc_kernel<false, false, true, false> : prefill_tc_kernel<false, false, false, false>;
 }
 
 int prefill_init() {
-    for (int i = 0; i < 8; ++i) {
-        if ((i & 1) && (i & 2)) continue;   // pre-rotated pages are never doc-local
-        if (cudaFuncSetAttribute(prefill_kernel_for(i & 1, i & 2, i & 4), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+    for (int i = 0; i < 9; ++i) {
+        if (i < 8 && (i & 1) && (i & 2)) continue;   // pre-rotated pages are never doc-local
+        PrefillKernel k = i == 8 ? prefill_kernel_for(false, false, false, true)
+                                 : prefill_kernel_for(i & 1, i & 2, i & 4, false);
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
             return LAZYATTN_ECUDA;
     }
     return LAZYATTN_OK;
@@ -758,7 +777,8 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     const int TQ = kRows / g;
     dim3 grid((b.max_q_len + TQ - 1) / TQ, p.d.n_kv_heads, b.num_requests);
     auto kern = prefill_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0,
-                                   p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0);
+                                   p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0,
+                                   p.d.position_encoding == LAZYATTN_POS_ALIBI);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }

@@ -112,6 +112,10 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     if (!d.k_pool || !d.v_pool || !d.rope_table || !d.status_word) return LAZYATTN_EINVAL;
     if (d.rope_scaling < LAZYATTN_ROPE_DEFAULT || d.rope_scaling > LAZYATTN_ROPE_LLAMA3) return LAZYATTN_EINVAL;
     if (d.rope_interleaved != 0 && !(d.rope_interleaved == 1 && d.dtype == LAZYATTN_BF16)) return LAZYATTN_EINVAL;
+    if (d.position_encoding != LAZYATTN_POS_ROPE &&
+        !(d.position_encoding == LAZYATTN_POS_ALIBI && d.dtype == LAZYATTN_BF16 && d.rope_scaling == 0 &&
+          d.rope_interleaved == 0 && d.key_storage == LAZYATTN_KEYS_POSITION_FREE))
+        return LAZYATTN_EINVAL;
     if (d.key_storage != LAZYATTN_KEYS_POSITION_FREE &&
         !(d.key_storage == LAZYATTN_KEYS_DOC_LOCAL && d.dtype == LAZYATTN_BF16))
         return LAZYATTN_EINVAL;
@@ -248,6 +252,7 @@ static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int o
     if (pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL &&
         ((b->flags & LAZYATTN_KEYS_PREROTATED) || (b->max_entries > 0 && !b->entry_delta)))
         return LAZYATTN_EINVAL;
+    if (pool->d.position_encoding == LAZYATTN_POS_ALIBI && (b->flags & LAZYATTN_KEYS_PREROTATED)) return LAZYATTN_EINVAL;
     if (op == LAZYATTN_OP_PREFILL) {
         if (b->total_q < 0 || b->max_q_len < 0 || !b->q_offsets || !b->q_start) return LAZYATTN_EINVAL;
     }
@@ -308,7 +313,7 @@ int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch, cons
     int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
     if (rc != LAZYATTN_OK) return rc;
     if (!dst_entries || (batch->flags & LAZYATTN_KEYS_PREROTATED) ||
-        pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL)
+        pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL || pool->d.position_encoding == LAZYATTN_POS_ALIBI)
         return LAZYATTN_EINVAL;
     if (batch->max_entries == 0) return LAZYATTN_OK;
     return launch_materialize(*pool, *batch, dst_entries, static_cast<cudaStream_t>(stream));

@@ -27,6 +27,8 @@ LAZYATTN_ROPE_YARN = 3
 LAZYATTN_ROPE_LLAMA3 = 4
 LAZYATTN_KEYS_POSITION_FREE = 0
 LAZYATTN_KEYS_DOC_LOCAL = 1
+LAZYATTN_POS_ROPE = 0
+LAZYATTN_POS_ALIBI = 1
 
 STATUS = {
     0: "LAZYATTN_OK", -1: "LAZYATTN_EINVAL", -2: "LAZYATTN_ENOSPC", -3: "LAZYATTN_ERANGE",
@@ -51,6 +53,7 @@ class lazyattn_pool_desc(ctypes.Structure):
         ("rope_scaling", ctypes.c_int32), ("rope_original_max_position", ctypes.c_int32),
         ("rope_factor", ctypes.c_double), ("rope_low", ctypes.c_double), ("rope_high", ctypes.c_double),
         ("key_storage", ctypes.c_int32), ("rope_interleaved", ctypes.c_int32),
+        ("position_encoding", ctypes.c_int32),
     ]
 
 

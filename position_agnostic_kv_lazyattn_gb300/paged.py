@@ -43,13 +43,15 @@ class Segment:
 class DevicePool:
     def __init__(self, num_pages: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: str,
                  rope_theta: float, max_position: int, device="cuda", stream=None, rope_scaling=None,
-                 key_storage: str = "position_free", rope_interleaved: bool = False):
+                 key_storage: str = "position_free", rope_interleaved: bool = False,
+                 position_encoding: str = "rope"):
         """rope_scaling: None (plain RoPE) or a dict with "kind" in {"linear", "ntk",
         "yarn", "llama3"}, "factor" and, for yarn / llama3, "original_max_position",
         "low", "high" (see lazyattn.h). key_storage: "position_free" (keys stored
         without RoPE) or "doc_local" (the paper's layout: keys stored rotated at
         document-local positions; bf16 only). rope_interleaved: q and k use
-        interleaved RoPE pairs (2i, 2i+1) (bf16 only)."""
+        interleaved RoPE pairs (2i, 2i+1) (bf16 only). position_encoding: "rope" or
+        "alibi" (no rotation; score bias -slope_h (m - n); bf16 only)."""
         self.dtype = dtype
         self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
@@ -76,6 +78,7 @@ class DevicePool:
             self.desc.rope_high = float(rope_scaling.get("high", 0.0))
         self.key_storage = key_storage
         self.desc.rope_interleaved = int(bool(rope_interleaved))
+        self.desc.position_encoding = {"rope": L.LAZYATTN_POS_ROPE, "alibi": L.LAZYATTN_POS_ALIBI}[position_encoding]
         self.desc.key_storage = {"position_free": L.LAZYATTN_KEYS_POSITION_FREE,
                                  "doc_local": L.LAZYATTN_KEYS_DOC_LOCAL}[key_storage]
         self.handle = L.lazyattn_pool_create(self.desc, stream)

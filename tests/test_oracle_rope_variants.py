@@ -121,3 +121,38 @@ def test_interleaved_scores_equal_half_pairing_on_permuted_vectors():
         a = oracle.rope(q, m, inter) @ oracle.rope(k, n, inter)
         b = oracle.rope(q[perm], m, BASE) @ oracle.rope(k[perm], n, BASE)
         assert a == pytest.approx(b, rel=1e-12, abs=1e-12)
+
+
+# ---------------------------------------------------------------- ALiBi (§3.5)
+
+def test_alibi_slopes_closed_forms():
+    """The slope rule of the ALiBi paper: geometric 2^(-8i/n) for powers of two;
+    for 12 heads the 8-head sequence then 2^-0.5, 2^-1.5, 2^-2.5, 2^-3.5."""
+    np.testing.assert_array_equal(oracle.alibi_slopes(8), [2.0 ** -i for i in range(1, 9)])
+    np.testing.assert_allclose(oracle.alibi_slopes(12),
+                               [2.0 ** -i for i in range(1, 9)] + [2.0 ** -(i + 0.5) for i in range(4)], rtol=1e-15)
+    s32 = oracle.alibi_slopes(32)
+    np.testing.assert_allclose(s32, [2.0 ** (-i / 4) for i in range(1, 33)], rtol=1e-15)
+    assert len(oracle.alibi_slopes(24)) == 24
+
+
+def test_alibi_attention_bruteforce_and_shift():
+    """Scores by explicit loops (no rotation, bias -slope (m - n), causal), and
+    invariance under a common shift of all positions."""
+    rng = np.random.default_rng(5)
+    Lq, L, Hq, Hkv, Dm = 3, 7, 4, 2, 16
+    q = rng.standard_normal((Lq, Hq, Dm))
+    k = rng.standard_normal((L, Hkv, Dm))
+    v = rng.standard_normal((L, Hkv, Dm))
+    qp, kp = np.arange(4, 7), np.arange(7)
+    got = oracle.attention(q, k, v, qp, kp, oracle.AlibiSpec())
+    slopes = oracle.alibi_slopes(Hq)
+    for i in range(Lq):
+        for h in range(Hq):
+            kv = h // (Hq // Hkv)
+            sc = [q[i, h] @ k[j, kv] / np.sqrt(Dm) - slopes[h] * (qp[i] - kp[j]) for j in range(L) if kp[j] <= qp[i]]
+            p = np.exp(np.array(sc) - max(sc))
+            want = (p / p.sum()) @ v[: len(sc), kv]
+            np.testing.assert_allclose(got[i, h], want, rtol=1e-12, atol=1e-12)
+    shifted = oracle.attention(q, k, v, qp + 1000, kp + 1000, oracle.AlibiSpec())
+    np.testing.assert_allclose(shifted, got, rtol=1e-9, atol=1e-12)

@@ -21,7 +21,8 @@ def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
 
 
 def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool = False,
-          extra_pages: int = 0, device="cuda", all_docs: bool = True, key_storage: str = "position_free"):
+          extra_pages: int = 0, device="cuda", all_docs: bool = True, key_storage: str = "position_free",
+          position_encoding: str = "rope"):
     """Build pool + tables for `requests` (default: all) of cfg.
 
     all_docs=False stores only the documents those requests use (the pool is
@@ -39,7 +40,7 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     base_pages = R * (cfg.docs_per_request * cfg.doc_pages + per_req) if baseline else 0
     num_pages = cfg.n_docs * cfg.doc_pages + R * per_req + base_pages + extra_pages
     pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
-                      cfg.max_position, device, key_storage=key_storage)
+                      cfg.max_position, device, key_storage=key_storage, position_encoding=position_encoding)
     doc_ids = range(cfg.n_docs) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
     doc_pages = {}
     for d in doc_ids:
