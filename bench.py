@@ -76,12 +76,14 @@ def measured_traffic(workload, kind):
 
 def work_model(cfg):
     """Algorithmic bytes / FLOPs of one step of cfg (all requests)."""
-    R, Hkv, Hq, D = cfg.n_requests, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
+    import workload
+    Hkv, Hq, D = cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
     esz = 4 if cfg.dtype == "f32" else 2
-    L0, Lq = cfg.context_len, cfg.q_len
-    pairs = Lq * L0 + Lq * (Lq + 1) // 2              # visible (query, key) pairs per head
-    prefill_flops = 4.0 * D * pairs * Hq * R
-    dec_bytes = [2.0 * (L0 + Lq + t + 1) * Hkv * D * esz * R for t in range(cfg.decode_steps)]
+    L0 = workload.request_context_lens(cfg)            # document tokens of each request
+    Lq = cfg.q_len
+    pairs = float(np.sum(Lq * L0 + Lq * (Lq + 1) // 2))   # visible (query, key) pairs per head, all requests
+    prefill_flops = 4.0 * D * pairs * Hq
+    dec_bytes = [2.0 * float(np.sum(L0 + Lq + t + 1)) * Hkv * D * esz for t in range(cfg.decode_steps)]
     return prefill_flops, dec_bytes
 
 
@@ -377,7 +379,8 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(local["step_ms"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "requests": R, "docs_per_request": cfg.docs_per_request,
-                   "doc_len": cfg.doc_len, "pool_docs": cfg.n_docs, "q_heads": cfg.n_q_heads,
+                   "doc_len": (f"{cfg.doc_len_min}..{cfg.doc_len}" if cfg.doc_len_min else cfg.doc_len),
+                   "pool_docs": cfg.n_docs, "q_heads": cfg.n_q_heads,
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "query_len": cfg.q_len,
                    "decode_steps": cfg.decode_steps, "zipf_alpha": cfg.zipf_alpha, "seed": cfg.seed,
                    "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
@@ -453,7 +456,8 @@ def cpu_baseline(cfg, budget_s=15.0, n_steps=None):
         st = [tuple(a[0] for a in workload.decode_inputs(cfg, t, [r])) for t in range(steps)]
         ts = time.perf_counter()
         oracle.decode_request(ctx, kq, vq, st, cfg.rope_theta)
-        nbytes += sum(2.0 * (cfg.context_len + cfg.q_len + t + 1) * cfg.n_kv_heads * cfg.head_dim * esz
+        L0 = sum(a[0].shape[0] for a in ctx)
+        nbytes += sum(2.0 * (L0 + cfg.q_len + t + 1) * cfg.n_kv_heads * cfg.head_dim * esz
                       for t in range(steps))
         done_req += 1
         if time.perf_counter() - t0 > budget_s:

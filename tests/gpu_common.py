@@ -58,3 +58,22 @@ class Reference:
         _, kq, vq = self.qseg(r)
         steps = [tuple(a[0] for a in workload.decode_inputs(self.cfg, t, [r])) for t in range(n_steps)]
         return oracle.decode_request(self.ctx(r), kq, vq, steps, self.cfg.rope_theta)
+
+
+def run_decode(L, env, steps, batch=None):
+    """`steps` decode calls (append + attention) over env's requests; the
+    outputs of each step, [R][Hq][D] as float arrays."""
+    import torch
+    import workload.device  # noqa: F401
+    cfg = env.cfg
+    batch = batch or env.batch
+    nbytes = L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_DECODE, batch.c)
+    ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device="cuda")
+    out = torch.empty((len(env.requests), cfg.n_q_heads, cfg.head_dim), dtype=env.pool.tdtype, device="cuda")
+    outs = []
+    for t in range(steps):
+        q, k, v = workload.device.decode_step_tensors(cfg, t, env.requests)
+        L.lazyattn_decode(env.pool.handle, batch.c, q, k, v, out, ws, nbytes)
+        outs.append(out.float().cpu().numpy().copy())
+    torch.cuda.synchronize()
+    return outs

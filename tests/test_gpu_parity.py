@@ -48,7 +48,7 @@ def _resolve(L, env):
     return got, np.array(ref, dtype=np.int64).reshape(-1, 3)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "llama3_8b"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama3_8b", "tiny_ragged_fp32", "few_shot_skewed"])
 def test_resolve_bit_exact(L, name):
     cfg = workload.CONFIGS[name]
     env = workload.device.setup(cfg)

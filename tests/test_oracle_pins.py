@@ -192,10 +192,12 @@ def test_resolve_entries_fields():
         (7, 0, 100), (7, 1, 101), (7, 2, 102), (9, 0, 5), (9, 1, 6)]
 
 
-def test_tiny_config_against_bruteforce():
-    """The tiny fp32 workload (3 docs of 32 tokens + 16 query tokens): prefill
-    and 4 decode steps by direct summation."""
-    cfg = workload.CONFIGS["tiny_fp32"]
+@pytest.mark.parametrize("name", ["tiny_fp32", "tiny_ragged_fp32"])
+def test_tiny_config_against_bruteforce(name):
+    """The tiny fp32 workloads (3 docs of 32 tokens + 16 query tokens; 4 distinct
+    docs of 5..40 tokens + 21 query tokens): prefill and every decode step by
+    direct summation."""
+    cfg = workload.CONFIGS[name]
     docs = workload.request_docs(cfg)
     for r in range(cfg.n_requests):
         ctx = [workload.doc_kv(cfg, int(d)) for d in docs[r]]
@@ -203,7 +205,7 @@ def test_tiny_config_against_bruteforce():
         got = oracle.prefill_request(ctx, q, kq, vq, cfg.rope_theta)
         kk = np.concatenate([c[0] for c in ctx] + [kq])
         vv = np.concatenate([c[1] for c in ctx] + [vq])
-        L0 = cfg.context_len
+        L0 = sum(c[0].shape[0] for c in ctx)
         # brute force on two query rows (first and last) to keep it quick
         for i in (0, cfg.q_len - 1):
             ref = bf_attention([q[i].tolist()], kk.tolist(), vv.tolist(), [L0 + i],

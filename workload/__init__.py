@@ -9,7 +9,10 @@ Workload shapes follow the configurations the LazyAttention paper's RAG setting
 implies (LazyAttention: Efficient Retrieval-Augmented Generation with Deferred
 Positional Encoding, §2 "Hit-ratio impact under limited cache capacity": Zipf
 document popularity, p_i proportional to i^-alpha; §4.3: documents concatenated
-ahead of a query segment, no common preamble).
+ahead of a query segment, no common preamble). The few-shot configurations follow
+App. C.7 "Beyond RAG: Few-Shot Classification": short exemplar chunks of varying
+length recur across requests at different positions and in different orders,
+with skewed or uniform popularity.
 
 Every random piece is drawn from its own PCG64 stream keyed by
 (seed, tag, index...), so any single document, query segment or decode step can
@@ -32,6 +35,7 @@ _TAG_DOC = 1
 _TAG_REQ_DOCS = 2
 _TAG_QSEG = 3
 _TAG_DECODE = 4
+_TAG_DOC_LEN = 5
 
 
 @dataclasses.dataclass(frozen=True)
@@ -43,13 +47,15 @@ class Config:
     head_dim: int
     rope_theta: float
     n_docs: int             # documents in the pool
-    doc_len: int            # tokens per document
+    doc_len: int            # tokens per document (the maximum when doc_len_min is set)
     n_requests: int
     docs_per_request: int
     zipf_alpha: Optional[float]   # None: uniform draws
     q_len: int              # query-segment tokens per request (0: none)
     decode_steps: int
     seed: int
+    doc_len_min: int = 0    # > 0: document lengths uniform in [doc_len_min, doc_len]
+    distinct: bool = False  # documents of one request drawn without replacement, then shuffled
 
     @property
     def group(self) -> int:
@@ -57,6 +63,7 @@ class Config:
 
     @property
     def doc_pages(self) -> int:
+        """Pages of the longest document."""
         return -(-self.doc_len // PAGE_SIZE)
 
     @property
@@ -76,8 +83,12 @@ class Config:
 
     @property
     def context_len(self) -> int:
-        """Document tokens per request (all requests have the same count)."""
-        return self.docs_per_request * self.doc_len
+        """Document tokens per request: the count when all documents have one
+        length, else the largest over the requests (request_context_len gives
+        each request's own)."""
+        if not self.doc_len_min:
+            return self.docs_per_request * self.doc_len
+        return int(max(request_context_lens(self))) if self.n_requests else 0
 
     @property
     def max_position(self) -> int:
@@ -98,6 +109,17 @@ CONFIGS = {
     "ttft_sweep_40": Config("ttft_sweep_40", "bf16", 32, 8, 128, 5.0e5, 500, 1024, 32, 40, 1.2, 128, 0, 3),
     # Llama-3-70B-shaped attention layer, ~16.8 GB of pre-RoPE KV resident.
     "llama3_70b": Config("llama3_70b", "bf16", 64, 8, 128, 5.0e5, 4000, 1024, 64, 32, 0.8, 256, 128, 4),
+    # Few-shot classification: 128 prompts of 32 distinct exemplar chunks (32..96
+    # tokens each, so entries start off page boundaries and end in partial pages)
+    # from a pool of 1000, skewed (Zipf 1.0) or uniform popularity, then a 48-token
+    # item to classify and 4 generated label tokens.
+    "few_shot_skewed": Config("few_shot_skewed", "bf16", 32, 8, 128, 5.0e5, 1000, 96, 128, 32, 1.0, 48, 4, 5,
+                              doc_len_min=32, distinct=True),
+    "few_shot_uniform": Config("few_shot_uniform", "bf16", 32, 8, 128, 5.0e5, 1000, 96, 128, 32, None, 48, 4, 6,
+                               doc_len_min=32, distinct=True),
+    # The same pattern at the tiny fp32 shape (parity only).
+    "tiny_ragged_fp32": Config("tiny_ragged_fp32", "f32", 4, 2, 64, 1.0e4, 6, 40, 3, 4, None, 21, 5, 7,
+                               doc_len_min=5, distinct=True),
 }
 
 
@@ -154,12 +176,34 @@ def request_docs(cfg: Config) -> np.ndarray:
 
     Rank i maps to document id i-1. Draws are i.i.d. with replacement, so a
     document may appear in several requests and twice within one request.
+    With cfg.distinct, each request instead draws its documents without
+    replacement (Zipf or uniform weights, one after another) and then shuffles
+    them, so a chunk appears at most once per prompt, in a random order.
     """
     rng = _rng(cfg.seed, _TAG_REQ_DOCS)
     shape = (cfg.n_requests, cfg.docs_per_request)
+    if cfg.distinct:
+        p = None if cfg.zipf_alpha is None else zipf_probabilities(cfg.n_docs, cfg.zipf_alpha)
+        out = np.empty(shape, np.int64)
+        for r in range(cfg.n_requests):
+            out[r] = rng.permutation(rng.choice(cfg.n_docs, size=cfg.docs_per_request, replace=False, p=p))
+        return out
     if cfg.zipf_alpha is None:
         return rng.integers(0, cfg.n_docs, size=shape).astype(np.int64)
     return zipf_ranks(rng, cfg.n_docs, cfg.zipf_alpha, shape) - 1
+
+
+def doc_lengths(cfg: Config) -> np.ndarray:
+    """Token count of every pool document (all cfg.doc_len unless doc_len_min is set)."""
+    if not cfg.doc_len_min:
+        return np.full(cfg.n_docs, cfg.doc_len, np.int64)
+    rng = _rng(cfg.seed, _TAG_DOC_LEN)
+    return rng.integers(cfg.doc_len_min, cfg.doc_len + 1, size=cfg.n_docs).astype(np.int64)
+
+
+def request_context_lens(cfg: Config) -> np.ndarray:
+    """Document tokens of each request."""
+    return doc_lengths(cfg)[request_docs(cfg)].sum(axis=1).astype(np.int64)
 
 
 # ----------------------------------------------------------------------------
@@ -167,9 +211,10 @@ def request_docs(cfg: Config) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def doc_kv(cfg: Config, doc_id: int):
-    """Pre-RoPE (k, v) of one document: two [doc_len][n_kv_heads][head_dim] arrays."""
+    """Pre-RoPE (k, v) of one document: two [length][n_kv_heads][head_dim] arrays."""
     rng = _rng(cfg.seed, _TAG_DOC, doc_id)
-    shape = (cfg.doc_len, cfg.n_kv_heads, cfg.head_dim)
+    n = cfg.doc_len if not cfg.doc_len_min else int(doc_lengths(cfg)[doc_id])
+    shape = (n, cfg.n_kv_heads, cfg.head_dim)
     return _normal(rng, shape, cfg.dtype), _normal(rng, shape, cfg.dtype)
 
 
@@ -202,15 +247,14 @@ def decode_inputs(cfg: Config, step: int, requests: Optional[Sequence[int]] = No
     return np.stack(qs), np.stack(ks), np.stack(vs)
 
 
-def request_layout(cfg: Config) -> List[int]:
-    """Logical start position of each document slot, then of the query segment.
+def request_layout(cfg: Config, r: int = 0) -> List[int]:
+    """Logical start position of each of request r's documents, then of its query segment.
 
     Documents are concatenated in table order from position 0 with no gaps; the
     query segment follows them; generated tokens follow the query segment.
     """
-    starts = [i * cfg.doc_len for i in range(cfg.docs_per_request)]
-    starts.append(cfg.context_len)
-    return starts
+    lens = doc_lengths(cfg)[request_docs(cfg)[r]]
+    return [0] + np.cumsum(lens).astype(np.int64).tolist()
 
 
 def shard_requests(n_requests: int, rank: int, world: int) -> List[int]:

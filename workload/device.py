@@ -12,7 +12,7 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import Config, PAGE_SIZE, decode_inputs, doc_kv, query_segment, request_docs
+from . import Config, PAGE_SIZE, decode_inputs, doc_kv, doc_lengths, query_segment, request_docs, request_layout
 
 
 def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
@@ -36,9 +36,11 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     reqs = list(range(cfg.n_requests)) if requests is None else list(requests)
     docs = request_docs(cfg)
     R = len(reqs)
+    lens = doc_lengths(cfg)
+    dpages = -(-lens // PAGE_SIZE)
     per_req = cfg.q_pages + cfg.decode_pages
-    base_pages = R * (cfg.docs_per_request * cfg.doc_pages + per_req) if baseline else 0
-    num_pages = cfg.n_docs * cfg.doc_pages + R * per_req + base_pages + extra_pages
+    base_pages = sum(int(dpages[docs[r]].sum()) + per_req for r in reqs) if baseline else 0
+    num_pages = int(dpages.sum()) + R * per_req + base_pages + extra_pages
     pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
                       cfg.max_position, device, key_storage=key_storage, position_encoding=position_encoding)
     doc_ids = range(cfg.n_docs) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
@@ -46,22 +48,25 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     for d in doc_ids:
         k, v = doc_kv(cfg, d)
         doc_pages[d] = pool.store_doc(to_device(k, cfg.dtype, device), to_device(v, cfg.dtype, device))
-    segs, qs = [], []
+    segs, qs, q_starts = [], [], []
     for r in reqs:
         s = []
+        starts = request_layout(cfg, r)
         for i, d in enumerate(docs[r]):
-            s.append(Segment(doc_pages[int(d)], i * cfg.doc_len, cfg.doc_len, False))
+            s.append(Segment(doc_pages[int(d)], starts[i], int(lens[d]), False))
+        ctx = starts[-1]
         if cfg.q_len:
             q, kq, vq = query_segment(cfg, r)
             qs.append(q)
             pages = pool.store_doc(to_device(kq, cfg.dtype, device), to_device(vq, cfg.dtype, device))
-            s.append(Segment(pages, cfg.context_len, cfg.q_len, True))
+            s.append(Segment(pages, ctx, cfg.q_len, True))
+            q_starts.append(ctx)
         if cfg.decode_pages:
             pages = pool.alloc_pages(cfg.decode_pages)
-            s.append(Segment(pages, cfg.context_len + cfg.q_pages * PAGE_SIZE, 0, True))
+            s.append(Segment(pages, ctx + cfg.q_pages * PAGE_SIZE, 0, True))
         segs.append(s)
     q_lens = [cfg.q_len] * R if cfg.q_len else []
-    batch = Batch(segs, q_lens, [cfg.context_len] * R if cfg.q_len else [], device)
+    batch = Batch(segs, q_lens, q_starts, device)
     q = to_device(np.concatenate(qs), cfg.dtype, device) if qs else None
     torch.cuda.synchronize()
     return types.SimpleNamespace(cfg=cfg, pool=pool, batch=batch, q=q, requests=reqs, docs=docs,
