@@ -53,8 +53,10 @@ KERNEL_SOURCES = {
     "prefill": ["k_prefill_tc.cu", "internal.h", "tc_ptx.cuh"],
 }
 NCU_TRAFFIC = {
-    ("llama3_8b", "decode"): (69.35e6, "d20b04487f59fa2d"),
-    ("llama3_8b", "prefill"): (78.13e6, "15537909d79a382a"),
+    ("llama3_8b", "decode"): (69.29e6, "8e76fd42a40b2f1d"),
+    ("llama3_8b", "prefill"): (78.09e6, "3bff3d06b457dd0e"),
+    ("few_shot_skewed", "decode"): (493.37e6, "8e76fd42a40b2f1d"),
+    ("few_shot_skewed", "prefill"): (598.99e6, "3bff3d06b457dd0e"),
 }
 
 
