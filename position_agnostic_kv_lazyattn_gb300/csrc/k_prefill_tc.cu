@@ -622,32 +622,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[i] = (m >> (i & 31)) & 1u ? v[i] : 0xff800000u;
                 }
             };
-            // ALiBi bias of key i of half hh (log2 domain; masked keys stay -inf)
-            auto add_bias = [&](uint32_t (&v)[64], int hh) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    // the page's start from the tile info (valid until this warp's P arrival)
-                    const float bp = alibi_c1 * (float)(info.start[4 * hh + q] - m_row);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        v[16 * q + i] = __float_as_uint(__uint_as_float(v[16 * q + i]) + fmaf(alibi_c1, (float)i, bp));
-                }
-            };
+            // ALiBi (log2 domain): key i of page q of half hh gets alibi_c1 * (start_q + i - m_row).
+            // The page's start comes from the tile info (valid until this warp's P arrival).
+            auto page_delta = [&](int hh, int q) { return info.start[4 * hh + q] - m_row; };
             // pass 1: row maximum over the tile
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+            // ALiBi: the reference maximum only has to bound the biased scores
+            // from above (it moves by kRescaleThreshold steps anyway), so each
+            // page's raw maximum takes the page's largest bias over visible keys,
+            // alibi_c1 * min(start + 15 - m_row, 0) (visible keys have n <= m_row).
+            float mxa = -INFINITY;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
                 if (!wfull) mask64(v, hh);
-                if (ALIBI) add_bias(v, hh);
+                if (ALIBI) {
+                    // per page (pairs 8q .. 8q+7), two chains each
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    for (int q = 0; q < 4; ++q) {
+                        float a = -INFINITY, c = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            const int j = 8 * q + i;
+                            a = fmax3(a, __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                            c = fmax3(c, __uint_as_float(v[2 * j + 2]), __uint_as_float(v[2 * j + 3]));
+                        }
+                        mxa = fmax3(mxa, a + alibi_c1 * (float)min(page_delta(hh, q) + 15, 0),
+                                    c + alibi_c1 * (float)min(page_delta(hh, q) + 15, 0));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        mx8[j & 7] = fmax3(mx8[j & 7], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                }
             }
-            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+            const float mx = ALIBI ? mxa
+                                   : fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                           fmaxf(mx8[6], mx8[7]));
             float alpha = 1.f;
             if (mx > m_run + kRescaleThreshold) {
                 alpha = fast_exp2(m_run - mx);   // 0 when m_run is -inf
@@ -675,14 +689,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[64];
                 tmem_ld64(ts + 64 * hh, v);
                 if (!wfull) mask64(v, hh);
-                if (ALIBI) add_bias(v, hh);
                 uint32_t pk[32];
+                if (ALIBI) {
+                    // exponent = s + bias - mref; (bias - mref) of keys 2i, 2i+1 of a
+                    // page stepped by 2 * alibi_c1 (masked keys stay -inf)
+                    const float2 step = make_float2(2.f * alibi_c1, 2.f * alibi_c1);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float2 d = sub2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref);
-                    const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                    sum4[j & 3] = add2(sum4[j & 3], pp);
-                    pk[j] = pack_bf2(pp.x, pp.y);
+                    for (int q = 0; q < 4; ++q) {
+                        const float k0 = fmaf(alibi_c1, (float)page_delta(hh, q), -mref);
+                        float2 w = make_float2(k0, k0 + alibi_c1);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int j = 8 * q + i;
+                            const float2 d = add2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), w);
+                            w = add2(w, step);
+                            const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                            sum4[j & 3] = add2(sum4[j & 3], pp);
+                            pk[j] = pack_bf2(pp.x, pp.y);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 d = sub2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref);
+                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        sum4[j & 3] = add2(sum4[j & 3], pp);
+                        pk[j] = pack_bf2(pp.x, pp.y);
+                    }
                 }
                 tmem_st32(ts + 32 * hh, pk);
             }
