@@ -72,7 +72,8 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
 /* Pool description. All pointers are device pointers owned by the caller.
  *   num_pages     pages in each of k_pool / v_pool (>= 1)
  *   page_size     must be LAZYATTN_PAGE_SIZE (16)
- *   n_q_heads     Hq; n_kv_heads Hkv; Hq % Hkv == 0
+ *   n_q_heads     Hq; n_kv_heads Hkv; Hq % Hkv == 0; for LAZYATTN_BF16 also Hq / Hkv <= 8
+ *                 (decode packs the query heads of one KV head into one 8-wide MMA tile)
  *   head_dim      D: 64 or 128 for LAZYATTN_F32; 128 for LAZYATTN_BF16
  *   dtype         element type of the pools, q, k_new, v_new and out
  *   rope_theta    RoPE base (> 0), frequencies theta^(-2i/D), i < D/2
@@ -156,7 +157,7 @@ typedef struct lazyattn_pool_desc {
 typedef struct lazyattn_pool* lazyattn_pool_t;
 
 /* A batch of requests. Device arrays unless stated otherwise.
- *   num_requests   R >= 1 (host value)
+ *   num_requests   1 <= R <= 65535 (host value; requests index a grid dimension)
  *   max_entries    host upper bound on entries per request (grid sizing)
  *   max_q_len      prefill: host upper bound on query tokens per request; decode: unused
  *   total_q        prefill: number of rows of q / out (host value); decode: unused

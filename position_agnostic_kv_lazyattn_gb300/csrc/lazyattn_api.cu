@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "internal.h"
@@ -166,12 +167,31 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     std::vector<double> inv(half);
     p->qk_scale = (float)(1.0 / sqrt((double)d.head_dim));
     rope_frequencies(d, inv.data(), &p->qk_scale);
-    for (int32_t pos = 0; pos < d.max_position; ++pos) {
-        float2* row = &tab[(size_t)pos * half];
-        for (int i = 0; i < half; ++i) {
-            const double a = (double)pos * inv[i];
-            row[i] = make_float2((float)cos(a), (float)sin(a));
+    auto fill_rows = [&](int32_t lo, int32_t hi) {
+        for (int32_t pos = lo; pos < hi; ++pos) {
+            float2* row = &tab[(size_t)pos * half];
+            for (int i = 0; i < half; ++i) {
+                const double a = (double)pos * inv[i];
+                row[i] = make_float2((float)cos(a), (float)sin(a));
+            }
         }
+    };
+    // long tables (millions of positions) are filled by several host threads
+    const int32_t kRowsPerThread = 1 << 16;
+    const int n_threads = (int)std::min<int64_t>(std::max(1u, std::thread::hardware_concurrency()),
+                                                 std::min<int64_t>(16, ((int64_t)d.max_position + kRowsPerThread - 1) /
+                                                                           kRowsPerThread));
+    if (n_threads <= 1) {
+        fill_rows(0, d.max_position);
+    } else {
+        std::vector<std::thread> pool_threads;
+        const int64_t per = ((int64_t)d.max_position + n_threads - 1) / n_threads;
+        for (int t = 0; t < n_threads; ++t) {
+            const int32_t lo = (int32_t)std::min<int64_t>((int64_t)t * per, d.max_position);
+            const int32_t hi = (int32_t)std::min<int64_t>((int64_t)(t + 1) * per, d.max_position);
+            pool_threads.emplace_back(fill_rows, lo, hi);
+        }
+        for (auto& th : pool_threads) th.join();
     }
     cudaError_t e = cudaMemcpyAsync(d.rope_table, tab.data(), tab.size() * sizeof(float2),
                                     cudaMemcpyHostToDevice, st);
@@ -247,7 +267,8 @@ int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32
 
 static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int op) {
     if (!pool || !b) return LAZYATTN_EINVAL;
-    if (b->num_requests < 1 || b->max_entries < 0 || !b->entries || !b->entry_offsets) return LAZYATTN_EINVAL;
+    if (b->num_requests < 1 || b->num_requests > 65535 || b->max_entries < 0 || !b->entries || !b->entry_offsets)
+        return LAZYATTN_EINVAL;
     if (b->flags & ~LAZYATTN_KEYS_PREROTATED) return LAZYATTN_EINVAL;
     if (pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL &&
         ((b->flags & LAZYATTN_KEYS_PREROTATED) || (b->max_entries > 0 && !b->entry_delta)))

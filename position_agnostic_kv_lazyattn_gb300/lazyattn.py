@@ -15,6 +15,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "liblazyattn.so")
 
 PAGE_SIZE = 16
+LAZYATTN_PAGE_SIZE = PAGE_SIZE
+LAZYATTN_MAX_START = (1 << 26) - 1
 LAZYATTN_F32 = 0
 LAZYATTN_BF16 = 1
 LAZYATTN_KEYS_PREROTATED = 1
@@ -35,6 +37,8 @@ STATUS = {
     -4: "LAZYATTN_EDTYPE", -5: "LAZYATTN_ECUDA", -6: "LAZYATTN_EDEVICE", -7: "LAZYATTN_EWORKSPACE",
     -8: "LAZYATTN_ENODECODE",
 }
+(LAZYATTN_OK, LAZYATTN_EINVAL, LAZYATTN_ENOSPC, LAZYATTN_ERANGE, LAZYATTN_EDTYPE, LAZYATTN_ECUDA, LAZYATTN_EDEVICE,
+ LAZYATTN_EWORKSPACE, LAZYATTN_ENODECODE) = (0, -1, -2, -3, -4, -5, -6, -7, -8)
 
 
 class LazyAttnError(RuntimeError):
@@ -106,6 +110,7 @@ EXPORTS = [
     "lazyattn_materialize", "lazyattn_resolve", "lazyattn_get_device_status", "lazyattn_decode_noalloc",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
+LAZYATTN_NOALLOC_SCRATCH_BYTES = NOALLOC_SCRATCH_BYTES
 
 
 def _check(rc: int, where: str):

@@ -55,6 +55,20 @@ def test_status_strings(L):
     assert L.lazyattn_status_string(-99) == "unknown status"
 
 
+def test_binding_constants_match_the_header(L):
+    """Every LAZYATTN_* integer constant of the header (#define or enum value)
+    has the same value in the Python binding."""
+    txt = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "lazyattn.h")).read(), flags=re.S)
+    found = {}
+    for name, expr in re.findall(r"#define\s+(LAZYATTN_[A-Z0-9_]+)\s+([-()\d\s<u]+)\n", txt):
+        found[name] = eval(expr.replace("u", ""), {})      # integer literals, shifts, minus only
+    found.update((n, int(v)) for n, v in re.findall(r"\b(LAZYATTN_[A-Z0-9_]+)\s*=\s*(-?\d+)", txt))
+    assert len(found) >= 25
+    for name, value in found.items():
+        assert hasattr(L, name), name
+        assert getattr(L, name) == value, name
+
+
 def test_rope_table_bytes(L):
     assert L.lazyattn_rope_table_bytes(128, 1000) == 1000 * 64 * 8
     assert L.lazyattn_rope_table_bytes(0, 10) == 0

@@ -49,7 +49,7 @@ def test_noalloc_decode_matches_workspace_decode(L, name, requests):
 def test_noalloc_rejects_batches_beyond_the_scratch_size(L):
     cfg = workload.CONFIGS["llama3_8b"]
     env = workload.device.setup(cfg, requests=[0], all_docs=False)
-    big = L.lazyattn_batch(200000, env.batch.max_entries, 0, 0, env.batch.entries.data_ptr(),
+    big = L.lazyattn_batch(60000, env.batch.max_entries, 0, 0, env.batch.entries.data_ptr(),
                            env.batch.entry_offsets.data_ptr(), None, None, 0)
     assert L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_DECODE, big) > L.lazyattn.NOALLOC_SCRATCH_BYTES
     dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
