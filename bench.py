@@ -52,6 +52,16 @@ KERNEL_SOURCES = {
     "decode": ["k_decode_bf16.cu", "k_paging.cu", "internal.h", "tc_ptx.cuh"],
     "prefill": ["k_prefill_tc.cu", "internal.h", "tc_ptx.cuh"],
 }
+# RoPE variants the bench can time: the kernels' work does not depend on the
+# values (only the position table and, for YaRN, the logit scale change).
+ROPE_PRESETS = {
+    "default": None,
+    "linear": dict(kind="linear", factor=4.0),
+    "ntk": dict(kind="ntk", factor=4.0),
+    "yarn": dict(kind="yarn", factor=4.0, original_max_position=2048, low=1.0, high=32.0),
+    "llama3": dict(kind="llama3", factor=8.0, original_max_position=8192, low=1.0, high=4.0),
+}
+
 NCU_TRAFFIC = {
     ("llama3_8b", "decode"): (69.32e6, "8e76fd42a40b2f1d"),
     ("llama3_8b", "prefill"): (77.93e6, "5556a5e9137526e2"),
@@ -155,7 +165,8 @@ def run_ours(args, rank, world):
         cfg = dataclasses.replace(cfg, n_requests=min(args.requests, cfg.n_requests))
     doc_local = args.keys == "doc_local" or args.pos == "alibi"   # no materialising baseline / no-RoPE leg
     env = wdev.setup(cfg, baseline=not args.no_extras and not doc_local, key_storage=args.keys,
-                     position_encoding=args.pos)
+                     position_encoding=args.pos, rope_scaling=ROPE_PRESETS[args.rope],
+                     rope_interleaved=args.interleaved)
     R = cfg.n_requests
     b = env.batch
     stream = torch.cuda.current_stream()
@@ -386,7 +397,8 @@ def run_ours(args, rank, world):
                    "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "query_len": cfg.q_len,
                    "decode_steps": cfg.decode_steps, "zipf_alpha": cfg.zipf_alpha, "seed": cfg.seed,
                    "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
-                   "keys": args.keys, "position_encoding": args.pos},
+                   "keys": args.keys, "position_encoding": args.pos, "rope": args.rope,
+                   "rope_interleaved": args.interleaved},
         "prefill_tflops": round(pre_tflops, 2), "ttft_ms": round(local["pre_ms"], 4),
         "decode_ms_per_token_step": round(mean_call, 4),
         "median_step_ms": round(statistics.median(step_ms), 4),
@@ -507,6 +519,9 @@ def main():
                     help="key layout: stored without RoPE (default) or rotated at document-local positions")
     ap.add_argument("--pos", default="rope", choices=["rope", "alibi"],
                     help="position encoding: RoPE (default) or the ALiBi score bias")
+    ap.add_argument("--rope", default="default", choices=list(ROPE_PRESETS),
+                    help="RoPE variant of the position table (presets in ROPE_PRESETS)")
+    ap.add_argument("--interleaved", action="store_true", help="interleaved RoPE pairs (2i, 2i+1)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -22,7 +22,7 @@ def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
 
 def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool = False,
           extra_pages: int = 0, device="cuda", all_docs: bool = True, key_storage: str = "position_free",
-          position_encoding: str = "rope"):
+          position_encoding: str = "rope", rope_scaling=None, rope_interleaved: bool = False):
     """Build pool + tables for `requests` (default: all) of cfg.
 
     all_docs=False stores only the documents those requests use (the pool is
@@ -30,6 +30,8 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     materialising baseline's private copies. key_storage selects the pool's key
     layout ("position_free" or "doc_local"); every stored run (a document, a
     query segment) is its own document, so its entries' delta is its start.
+    position_encoding, rope_scaling and rope_interleaved pass through to the
+    pool (see DevicePool).
     """
     from position_agnostic_kv_lazyattn_gb300 import Batch, DevicePool, Segment
 
@@ -42,7 +44,8 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     base_pages = sum(int(dpages[docs[r]].sum()) + per_req for r in reqs) if baseline else 0
     num_pages = int(dpages.sum()) + R * per_req + base_pages + extra_pages
     pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
-                      cfg.max_position, device, key_storage=key_storage, position_encoding=position_encoding)
+                      cfg.max_position, device, key_storage=key_storage, position_encoding=position_encoding,
+                      rope_scaling=rope_scaling, rope_interleaved=rope_interleaved)
     doc_ids = range(cfg.n_docs) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
     doc_pages = {}
     for d in doc_ids:
