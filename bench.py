@@ -63,9 +63,9 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    ("llama3_8b", "decode"): (69.32e6, "8e76fd42a40b2f1d"),
+    ("llama3_8b", "decode"): (69.24e6, "0331c289f3c50d9d"),
     ("llama3_8b", "prefill"): (77.93e6, "5556a5e9137526e2"),
-    ("few_shot_skewed", "decode"): (493.77e6, "8e76fd42a40b2f1d"),
+    ("few_shot_skewed", "decode"): (493.73e6, "0331c289f3c50d9d"),
     ("few_shot_skewed", "prefill"): (598.75e6, "5556a5e9137526e2"),
 }
 

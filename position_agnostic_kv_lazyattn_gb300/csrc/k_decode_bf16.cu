@@ -209,14 +209,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     __syncthreads();
     const int e0 = P.entry_offsets[r], e1 = P.entry_offsets[r + 1];   // not written by the append
-    grid_dep_wait();
-    const int m = P.qpos[r];
-    __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
-    if (m < 0) {   // request without an appended token (status already recorded)
-        if (s == 0)
-            for (int i = tid; i < g * kD; i += kThreads) out_rh[i] = __float2bfloat16_rn(0.f);
-        return;
-    }
+    int m = -1;   // logical position of the appended token: read from the append after grid_dep_wait()
 
     const int chunk = (e1 - e0 + S - 1) / S;
     const int cb = e0 + s * chunk;
@@ -258,12 +251,38 @@ __global__ void __launch_bounds__(kThreads, 3)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float4* rowbuf = reinterpret_cast<float4*>(sm + kBaseBufOff + warp * kRowBytes);
+    // The append writes only the writable entry it appends into and that
+    // entry's page; other entries, their pages and the position table are
+    // final already. So, where taking part does not depend on m (every layout
+    // but doc-local), the first pages of entries that are not writable are
+    // requested before waiting for the append, and their loads overlap it.
     uint64_t e_cur = entry_at(0), e_n1 = entry_at(1);
+    const bool early0 = !LOCAL && !entry_writable(e_cur);
+    const bool early1 = !LOCAL && !entry_writable(e_n1);
+    if (lane == 0) {
+        if (early0) issue(0, e_cur, 0);
+        if (early1) issue(1, e_n1, 0);
+    }
+    grid_dep_wait();
+    m = P.qpos[r];
+    __nv_bfloat16* out_rh = P.out + ((size_t)r * Hq + (size_t)h * g) * kD;
+    if (m < 0) {   // request without an appended token (status already recorded)
+        if (lane == 0) {   // the early copies land before the CTA's shared memory is released
+            volatile int never = 0;
+            if (early0 && 0 < n_w && page_n(e_cur, 0) > 0) mbar_wait(smem_u32(&bar_full[warp][0]), 0, &never);
+            if (early1 && 1 < n_w && page_n(e_n1, 0) > 0) mbar_wait(smem_u32(&bar_full[warp][1]), 0, &never);
+        }
+        if (s == 0)
+            for (int i = tid; i < g * kD; i += kThreads) out_rh[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    if (!early0) e_cur = entry_at(0);   // writable entries: read again, the append may have filled them
+    if (!early1) e_n1 = entry_at(1);
     int d_cur = delta_at(0), d_n1 = delta_at(1);
     float4 row_next = row_of(e_cur, d_cur);
     if (lane == 0) {
-        issue(0, e_cur, d_cur);
-        issue(1, e_n1, d_n1);
+        if (!early0) issue(0, e_cur, d_cur);
+        if (!early1) issue(1, e_n1, d_n1);
     }
 
     // (the first pages are in flight while q is read and rotated)
