@@ -121,7 +121,7 @@ struct DecodeWs {
 
 struct lazyattn_pool {
     lazyattn_pool_desc d;
-    std::vector<int32_t> free_stack;   // free page ids, lowest id on top
+    std::vector<int32_t> free_heap;    // free page ids, a min-heap (std::greater): lowest id first
     std::vector<uint8_t> is_free;
     int device = 0;
     int sm_count = 0;

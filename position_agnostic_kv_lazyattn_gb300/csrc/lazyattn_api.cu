@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <new>
 #include <thread>
 #include <vector>
@@ -140,8 +141,8 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     if (!p) return LAZYATTN_EINVAL;
     p->d = d;
     p->is_free.assign((size_t)d.num_pages, 1);
-    p->free_stack.resize((size_t)d.num_pages);
-    for (int32_t i = 0; i < d.num_pages; ++i) p->free_stack[(size_t)i] = d.num_pages - 1 - i;
+    p->free_heap.resize((size_t)d.num_pages);
+    for (int32_t i = 0; i < d.num_pages; ++i) p->free_heap[(size_t)i] = i;   // ascending: already a min-heap
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaGetDevice(&p->device) != cudaSuccess ||
@@ -213,16 +214,17 @@ int lazyattn_pool_destroy(lazyattn_pool_t pool) {
 
 int lazyattn_pool_free_count(lazyattn_pool_t pool, int32_t* out_count) {
     if (!pool || !out_count) return LAZYATTN_EINVAL;
-    *out_count = (int32_t)pool->free_stack.size();
+    *out_count = (int32_t)pool->free_heap.size();
     return LAZYATTN_OK;
 }
 
 int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages) {
     if (!pool || n < 0 || (n > 0 && !out_pages)) return LAZYATTN_EINVAL;
-    if ((size_t)n > pool->free_stack.size()) return LAZYATTN_ENOSPC;
+    if ((size_t)n > pool->free_heap.size()) return LAZYATTN_ENOSPC;
     for (int32_t i = 0; i < n; ++i) {
-        const int32_t pg = pool->free_stack.back();
-        pool->free_stack.pop_back();
+        std::pop_heap(pool->free_heap.begin(), pool->free_heap.end(), std::greater<int32_t>());
+        const int32_t pg = pool->free_heap.back();
+        pool->free_heap.pop_back();
         pool->is_free[(size_t)pg] = 0;
         out_pages[i] = pg;
     }
@@ -240,10 +242,12 @@ int lazyattn_free_pages(lazyattn_pool_t pool, const int32_t* pages, int32_t n) {
     }
     std::sort(seen.begin(), seen.end());
     if (std::adjacent_find(seen.begin(), seen.end()) != seen.end()) return LAZYATTN_EINVAL;
-    // Keep the stack ordered so that the lowest free id is handed out first.
-    for (int32_t pg : seen) pool->is_free[(size_t)pg] = 1;
-    pool->free_stack.insert(pool->free_stack.end(), seen.begin(), seen.end());
-    std::sort(pool->free_stack.begin(), pool->free_stack.end(), std::greater<int32_t>());
+    // O(log free) per page; the heap hands out the lowest free id first.
+    for (int32_t pg : seen) {
+        pool->is_free[(size_t)pg] = 1;
+        pool->free_heap.push_back(pg);
+        std::push_heap(pool->free_heap.begin(), pool->free_heap.end(), std::greater<int32_t>());
+    }
     return LAZYATTN_OK;
 }
 
