@@ -18,7 +18,7 @@ Positional Encoding.
     iterated rotation state.
   * §3.5 "GQA/MQA compatibility": query heads share KV heads; no other change.
 
-Readings where the paper is silent (each is listed in the design doc):
+Readings where the paper is silent:
   * pairing is rotate-half (dims i and i + D/2), as the paper's "half-dimensions"
     K1 / K2 of Figure 3(b) describe;
   * frequencies theta_i = base^(-2i/D) for i < D/2 (RoFormer's definition);
