@@ -185,13 +185,22 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     if (n_threads <= 1) {
         fill_rows(0, d.max_position);
     } else {
+        // Rows [lo, hi) per thread; rows whose thread could not be started are
+        // filled here (no exception leaves this C entry point).
         std::vector<std::thread> pool_threads;
         const int64_t per = ((int64_t)d.max_position + n_threads - 1) / n_threads;
+        int32_t done_upto = 0;   // rows [0, done_upto) are handed to started threads
         for (int t = 0; t < n_threads; ++t) {
             const int32_t lo = (int32_t)std::min<int64_t>((int64_t)t * per, d.max_position);
             const int32_t hi = (int32_t)std::min<int64_t>((int64_t)(t + 1) * per, d.max_position);
-            pool_threads.emplace_back(fill_rows, lo, hi);
+            try {
+                pool_threads.emplace_back(fill_rows, lo, hi);
+            } catch (...) {
+                break;
+            }
+            done_upto = hi;
         }
+        fill_rows(done_upto, d.max_position);
         for (auto& th : pool_threads) th.join();
     }
     cudaError_t e = cudaMemcpyAsync(d.rope_table, tab.data(), tab.size() * sizeof(float2),
