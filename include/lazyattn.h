@@ -209,7 +209,8 @@ size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position);
 /* Create a pool over caller-owned buffers. Validates desc, fills the position
  * table (fp64 on the host, stored fp32) and zeroes the status word on `stream`,
  * then synchronises that stream before returning. All pages start free.
- * Returns LAZYATTN_OK and *out_pool, or EINVAL/EDTYPE/ECUDA (nothing created). */
+ * Returns LAZYATTN_OK and *out_pool, or EINVAL/EDTYPE/ECUDA, or ENOSPC when the host
+ * memory for the pool's metadata or the position table cannot be had (nothing created). */
 int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_pool_t* out_pool);
 
 /* Release the host metadata of a pool (device buffers stay with the caller). */

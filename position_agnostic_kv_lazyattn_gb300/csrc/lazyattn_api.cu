@@ -138,10 +138,15 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     }
 
     lazyattn_pool* p = new (std::nothrow) lazyattn_pool();
-    if (!p) return LAZYATTN_EINVAL;
+    if (!p) return LAZYATTN_ENOSPC;
     p->d = d;
-    p->is_free.assign((size_t)d.num_pages, 1);
-    p->free_heap.resize((size_t)d.num_pages);
+    try {   // host memory only; no exception leaves this C entry point
+        p->is_free.assign((size_t)d.num_pages, 1);
+        p->free_heap.resize((size_t)d.num_pages);   // never grows past this: pushes cannot reallocate
+    } catch (...) {
+        delete p;
+        return LAZYATTN_ENOSPC;
+    }
     for (int32_t i = 0; i < d.num_pages; ++i) p->free_heap[(size_t)i] = i;   // ascending: already a min-heap
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -164,8 +169,15 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     // Position table: angle pos * theta_i in fp64, cos/sin in fp64, stored fp32;
     // theta_i from the pool's RoPE variant.
     const int half = d.head_dim / 2;
-    std::vector<float2> tab((size_t)d.max_position * (size_t)half);
-    std::vector<double> inv(half);
+    std::vector<float2> tab;
+    std::vector<double> inv;
+    try {
+        tab.resize((size_t)d.max_position * (size_t)half);
+        inv.resize((size_t)half);
+    } catch (...) {
+        delete p;
+        return LAZYATTN_ENOSPC;
+    }
     p->qk_scale = (float)(1.0 / sqrt((double)d.head_dim));
     rope_frequencies(d, inv.data(), &p->qk_scale);
     auto fill_rows = [&](int32_t lo, int32_t hi) {
@@ -242,19 +254,25 @@ int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages) {
 
 int lazyattn_free_pages(lazyattn_pool_t pool, const int32_t* pages, int32_t n) {
     if (!pool || n < 0 || (n > 0 && !pages)) return LAZYATTN_EINVAL;
-    std::vector<int32_t> seen;
-    seen.reserve((size_t)n);
-    for (int32_t i = 0; i < n; ++i) {
-        if (pages[i] < 0 || pages[i] >= pool->d.num_pages) return LAZYATTN_ERANGE;
-        if (pool->is_free[(size_t)pages[i]]) return LAZYATTN_EINVAL;
-        seen.push_back(pages[i]);
+    // Validate every id before changing anything: in range, taken, not repeated
+    // (repeats are found by marking each id once; marks are undone on failure).
+    constexpr uint8_t kMarked = 2;
+    int rc = LAZYATTN_OK;
+    int32_t marked = 0;
+    for (; marked < n; ++marked) {
+        const int32_t pg = pages[marked];
+        if (pg < 0 || pg >= pool->d.num_pages) { rc = LAZYATTN_ERANGE; break; }
+        if (pool->is_free[(size_t)pg]) { rc = LAZYATTN_EINVAL; break; }   // free, or repeated (marked)
+        pool->is_free[(size_t)pg] = kMarked;
     }
-    std::sort(seen.begin(), seen.end());
-    if (std::adjacent_find(seen.begin(), seen.end()) != seen.end()) return LAZYATTN_EINVAL;
+    if (rc != LAZYATTN_OK) {
+        for (int32_t i = 0; i < marked; ++i) pool->is_free[(size_t)pages[i]] = 0;
+        return rc;
+    }
     // O(log free) per page; the heap hands out the lowest free id first.
-    for (int32_t pg : seen) {
-        pool->is_free[(size_t)pg] = 1;
-        pool->free_heap.push_back(pg);
+    for (int32_t i = 0; i < n; ++i) {
+        pool->is_free[(size_t)pages[i]] = 1;
+        pool->free_heap.push_back(pages[i]);
         std::push_heap(pool->free_heap.begin(), pool->free_heap.end(), std::greater<int32_t>());
     }
     return LAZYATTN_OK;
