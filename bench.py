@@ -64,10 +64,10 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    ("llama3_8b", "decode"): (69.24e6, "0331c289f3c50d9d"),
-    ("llama3_8b", "prefill"): (77.93e6, "5556a5e9137526e2"),
-    ("few_shot_skewed", "decode"): (493.73e6, "0331c289f3c50d9d"),
-    ("few_shot_skewed", "prefill"): (598.75e6, "5556a5e9137526e2"),
+    ("llama3_8b", "decode"): (69.25e6, "b19624a9cee07e87"),
+    ("llama3_8b", "prefill"): (77.89e6, "0c435da0e4b12845"),
+    ("few_shot_skewed", "decode"): (494.20e6, "b19624a9cee07e87"),
+    ("few_shot_skewed", "prefill"): (599.04e6, "0c435da0e4b12845"),
 }
 
 
