@@ -1,0 +1,73 @@
+"""Host-side block tables (position_agnostic_kv_lazyattn_gb300.paged) on CPU:
+segments become the entries lazyattn_pack_entry defines (page, logical start of
+slot 0, valid slots, writable), requests get their entry ranges, document-local
+offsets default to each run's start, and the prefill query layout is the
+exclusive prefix sum of the query lengths. Entries are decoded with the oracle's
+own unpacking, which is pinned separately."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def P():
+    import __graft_entry__
+    __graft_entry__.build()
+    from position_agnostic_kv_lazyattn_gb300 import paged
+    return paged
+
+
+def test_ragged_segment_entries(P):
+    seg = P.Segment([5, 6, 7], start=66, n_tokens=37, writable=True)
+    pages, starts, nvalid, wr = P.segment_entries(seg)
+    assert (pages, starts, nvalid, wr) == ([5, 6, 7], [66, 82, 98], [16, 16, 5], [1, 1, 1])
+    # the tokens resolve to consecutive logical positions 66 .. 102
+    ent = P.pack_entries(pages, starts, nvalid, wr)
+    toks = oracle.resolve_entries([int(e) for e in ent])
+    assert [t[2] for t in toks] == list(range(66, 103))
+    assert [(t[0], t[1]) for t in toks][:17] == [(5, s) for s in range(16)] + [(6, 0)]
+    # a reserved page for generated tokens: no valid slot yet
+    _, starts, nvalid, _ = P.segment_entries(P.Segment([9], start=112, n_tokens=0, writable=True))
+    assert starts == [112] and nvalid == [0]
+    with pytest.raises(AssertionError):
+        P.segment_entries(P.Segment([1], start=0, n_tokens=17))   # more tokens than pages hold
+
+
+def test_batch_layout(P):
+    reqs = [
+        [P.Segment([0, 1], 0, 20), P.Segment([2], 20, 7, True)],
+        [P.Segment([3], 0, 16), P.Segment([0, 1], 16, 20, delta=10), P.Segment([4, 5], 36, 29, True)],
+        [P.Segment([6], 0, 5, True)],
+    ]
+    b = P.Batch(reqs, q_lens=[7, 29, 5], q_starts=[20, 36, 0], device="cpu")
+    assert b.num_requests == 3
+    assert b.offsets_host.tolist() == [0, 3, 8, 9]
+    assert b.max_entries == 5
+    assert b.total_q == 41 and b.max_q_len == 29
+    assert b.q_offsets.tolist() == [0, 7, 36, 41]
+    assert b.q_start.tolist() == [20, 36, 0]
+    got = [oracle.unpack_entry(int(e)) for e in b.entries_host]
+    assert got[3:8] == [(3, 0, 16, 0), (0, 16, 16, 0), (1, 32, 4, 0), (4, 36, 16, 1), (5, 52, 13, 1)]
+    # document-local offsets: a run's start unless given
+    assert b.delta_host.tolist() == [0, 0, 20, 0, 10, 10, 36, 36, 0]
+    # the same document (pages 0, 1) serves request 0 at 0 and request 1 at 16
+    r0 = oracle.resolve_entries([int(e) for e in b.entries_host[0:3]])
+    r1 = oracle.resolve_entries([int(e) for e in b.entries_host[3:8]])
+    assert [t[:2] for t in r0[:20]] == [t[:2] for t in r1[16:36]]
+    assert [t[2] for t in r1[16:36]] == list(range(16, 36))
+    # another entry array with the same requests and query layout (the baseline's copies)
+    dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.arange(100, 109, dtype=np.uint64)
+    mb = b.with_entries(dst, 1, device="cpu")
+    assert mb.flags == 1 and mb.offsets_host.tolist() == b.offsets_host.tolist()
+    assert [oracle.unpack_entry(int(e))[0] for e in mb.entries_host] == list(range(100, 109))
+    assert [oracle.unpack_entry(int(e))[1:] for e in mb.entries_host] == \
+        [oracle.unpack_entry(int(e))[1:] for e in b.entries_host]
+    assert torch.equal(mb.entry_offsets, b.entry_offsets)
+
+
+def test_decode_only_batch_has_no_query_layout(P):
+    b = P.Batch([[P.Segment([0], 0, 3, True)]], device="cpu")
+    assert b.q_offsets is None and b.total_q == 0 and b.max_q_len == 0
+    assert b.c.num_requests == 1 and b.c.max_entries == 1
