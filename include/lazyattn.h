@@ -295,6 +295,20 @@ int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch,
 int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const int32_t* out_offsets,
                      int32_t* out_triples, int32_t out_cap, void* stream);
 
+/* Host-side check of a block table before it is uploaded (a debug aid: the
+ * kernels only range-check entries, on the device, and skip what fails).
+ * entries / entry_offsets: HOST copies of a batch's arrays (int32 [R+1] offsets).
+ * For every request r, every entry with nvalid > 0 must name a page below
+ * num_pages, hold at most 16 valid slots and end at or below max_position
+ * (else LAZYATTN_ERANGE), and no two tokens of the request may share a logical
+ * position (else LAZYATTN_EINVAL): the request's entries describe one logical
+ * sequence, one token per position (§3.2). Entries may come in any order.
+ * Returns LAZYATTN_OK, or the failure with *out_request (if not NULL) set to the
+ * first failing request (-1 for malformed arguments: EINVAL). ENOSPC if host
+ * memory for the check cannot be had. Needs no GPU. */
+int lazyattn_check_batch_host(const uint64_t* entries, const int32_t* entry_offsets, int32_t num_requests,
+                              int32_t num_pages, int32_t max_position, int32_t* out_request);
+
 /* Copy the device status word to *out_status (synchronises `stream`), then
  * reset it to zero if reset != 0. 0 means no device-side error since the last
  * reset; otherwise a negative lazyattn_status. */

@@ -7,6 +7,7 @@
 #include <functional>
 #include <new>
 #include <thread>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -377,6 +378,48 @@ int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const in
     if (rc != LAZYATTN_OK) return rc;
     if (!out_offsets || !out_triples || out_cap < 0) return LAZYATTN_EINVAL;
     return launch_resolve(*pool, *batch, out_offsets, out_triples, out_cap, static_cast<cudaStream_t>(stream));
+}
+
+int lazyattn_check_batch_host(const uint64_t* entries, const int32_t* entry_offsets, int32_t num_requests,
+                              int32_t num_pages, int32_t max_position, int32_t* out_request) {
+    if (out_request) *out_request = -1;
+    if (!entry_offsets || num_requests < 0 || num_pages < 1 || max_position < 1) return LAZYATTN_EINVAL;
+    if (num_requests > 0 && entry_offsets[0] < 0) return LAZYATTN_EINVAL;
+    for (int32_t r = 0; r < num_requests; ++r)
+        if (entry_offsets[r + 1] < entry_offsets[r]) return LAZYATTN_EINVAL;
+    if (num_requests > 0 && entry_offsets[num_requests] > 0 && !entries) return LAZYATTN_EINVAL;
+    std::vector<std::pair<int64_t, int64_t>> spans;   // [start, start + nvalid) of one request
+    for (int32_t r = 0; r < num_requests; ++r) {
+        int rc = LAZYATTN_OK;
+        try {
+            spans.clear();
+            for (int32_t i = entry_offsets[r]; i < entry_offsets[r + 1]; ++i) {
+                const uint64_t e = entries[i];
+                const int32_t n = entry_nvalid(e);
+                if (n == 0) continue;
+                if (entry_page(e) >= (uint32_t)num_pages || n > kPage || entry_start(e) + n > max_position) {
+                    rc = LAZYATTN_ERANGE;
+                    break;
+                }
+                spans.emplace_back(entry_start(e), entry_start(e) + n);
+            }
+        } catch (...) {
+            return LAZYATTN_ENOSPC;
+        }
+        if (rc == LAZYATTN_OK) {
+            std::sort(spans.begin(), spans.end());
+            for (size_t i = 1; i < spans.size(); ++i)
+                if (spans[i].first < spans[i - 1].second) {
+                    rc = LAZYATTN_EINVAL;
+                    break;
+                }
+        }
+        if (rc != LAZYATTN_OK) {
+            if (out_request) *out_request = r;
+            return rc;
+        }
+    }
+    return LAZYATTN_OK;
 }
 
 int lazyattn_get_device_status(lazyattn_pool_t pool, int32_t* out_status, int32_t reset, void* stream) {

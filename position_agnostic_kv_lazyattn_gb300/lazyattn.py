@@ -94,6 +94,7 @@ def _load():
         "lazyattn_resolve": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp, i32, vp]),
         "lazyattn_get_device_status": (ctypes.c_int, [vp, P_i32, i32, vp]),
         "lazyattn_decode_noalloc": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp, vp, vp, vp]),
+        "lazyattn_check_batch_host": (ctypes.c_int, [vp, vp, i32, i32, i32, P_i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -108,6 +109,7 @@ EXPORTS = [
     "lazyattn_pool_destroy", "lazyattn_pool_free_count", "lazyattn_alloc_pages", "lazyattn_free_pages",
     "lazyattn_store_doc", "lazyattn_workspace_size", "lazyattn_prefill", "lazyattn_decode",
     "lazyattn_materialize", "lazyattn_resolve", "lazyattn_get_device_status", "lazyattn_decode_noalloc",
+    "lazyattn_check_batch_host",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 LAZYATTN_NOALLOC_SCRATCH_BYTES = NOALLOC_SCRATCH_BYTES
@@ -191,6 +193,18 @@ def make_batch(num_requests, max_entries, entries, entry_offsets, q_offsets=None
     """Fill a lazyattn_batch from device tensors (int64 entries, int32 offsets and deltas)."""
     return lazyattn_batch(num_requests, max_entries, max_q_len, total_q, _ptr(entries), _ptr(entry_offsets),
                           _ptr(q_offsets), _ptr(q_start), flags, _ptr(entry_delta))
+
+
+def lazyattn_check_batch_host(entries, entry_offsets, num_pages: int, max_position: int):
+    """Host check of a block table (numpy uint64 entries, int32 offsets [R+1]).
+    Returns (status, first failing request or -1); raises nothing."""
+    import numpy as np
+    e = np.ascontiguousarray(entries, dtype=np.uint64)
+    o = np.ascontiguousarray(entry_offsets, dtype=np.int32)
+    bad = ctypes.c_int32(-1)
+    rc = lib.lazyattn_check_batch_host(e.ctypes.data if e.size else None, o.ctypes.data, len(o) - 1, num_pages,
+                                       max_position, ctypes.byref(bad))
+    return rc, bad.value
 
 
 def lazyattn_workspace_size(pool: int, op: int, batch: lazyattn_batch) -> int:

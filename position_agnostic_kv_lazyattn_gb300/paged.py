@@ -155,6 +155,14 @@ class Batch:
         self.c = L.make_batch(self.num_requests, self.max_entries, self.entries, self.entry_offsets,
                               self.q_offsets, self.q_start, self.max_q_len, self.total_q, flags, self.entry_delta)
 
+    def check(self, num_pages: int, max_position: int):
+        """Host check of the table (lazyattn_check_batch_host): entries in range
+        and no two tokens of a request at one logical position. Raises
+        LazyAttnError naming the first failing request."""
+        rc, bad = L.lazyattn_check_batch_host(self.entries_host, self.offsets_host, num_pages, max_position)
+        if rc != 0:
+            raise L.LazyAttnError(rc, f"block table of request {bad}")
+
     def with_entries(self, entries_host: np.ndarray, flags: int, device="cuda") -> "Batch":
         """Same requests and query layout, another entry array (e.g. materialised pages)."""
         b = Batch.__new__(Batch)

@@ -71,3 +71,34 @@ def test_decode_only_batch_has_no_query_layout(P):
     b = P.Batch([[P.Segment([0], 0, 3, True)]], device="cpu")
     assert b.q_offsets is None and b.total_q == 0 and b.max_q_len == 0
     assert b.c.num_requests == 1 and b.c.max_entries == 1
+
+
+def test_host_table_check(P):
+    from position_agnostic_kv_lazyattn_gb300 import lazyattn as L
+    ok = P.Batch([[P.Segment([0, 1], 0, 20), P.Segment([2], 20, 7, True)],
+                  [P.Segment([3], 16, 16), P.Segment([0, 1], 32, 20), P.Segment([4], 0, 16)]],   # any order
+                 q_lens=[7, 0], q_starts=[20, 52], device="cpu")
+    ok.check(num_pages=8, max_position=64)
+    assert L.lazyattn_check_batch_host(ok.entries_host, ok.offsets_host, 8, 64) == (0, -1)
+    # an empty entry may sit anywhere (it holds no token)
+    P.Batch([[P.Segment([0], 0, 16), P.Segment([5], 8, 0, True)]], device="cpu").check(8, 64)
+
+    def status(reqs, num_pages=8, max_position=64):
+        b = P.Batch(reqs, device="cpu")
+        return L.lazyattn_check_batch_host(b.entries_host, b.offsets_host, num_pages, max_position)
+
+    good = [P.Segment([0], 0, 16)]
+    # two tokens of request 1 at positions 16..19
+    assert status([good, [P.Segment([0, 1], 0, 20), P.Segment([2], 16, 7)]]) == (L.LAZYATTN_EINVAL, 1)
+    # the same document twice at one offset
+    assert status([[P.Segment([0], 0, 10), P.Segment([0], 0, 10)]]) == (L.LAZYATTN_EINVAL, 0)
+    # page outside the pool; positions past the table
+    assert status([good, good, [P.Segment([8], 0, 3)]]) == (L.LAZYATTN_ERANGE, 2)
+    assert status([[P.Segment([1], 60, 5)]]) == (L.LAZYATTN_ERANGE, 0)
+    # more than 16 valid slots in one entry (the field holds up to 31)
+    e = P.pack_entries([1], [0], [17], [0])
+    assert L.lazyattn_check_batch_host(e, [0, 1], 8, 64) == (L.LAZYATTN_ERANGE, 0)
+    # malformed offsets
+    assert L.lazyattn_check_batch_host(e, [1, 0], 8, 64) == (L.LAZYATTN_EINVAL, -1)
+    with pytest.raises(L.LazyAttnError):
+        P.Batch([[P.Segment([0], 0, 10), P.Segment([1], 5, 10)]], device="cpu").check(8, 64)

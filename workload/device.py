@@ -70,6 +70,7 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
         segs.append(s)
     q_lens = [cfg.q_len] * R if cfg.q_len else []
     batch = Batch(segs, q_lens, q_starts, device)
+    batch.check(num_pages, cfg.max_position)   # every table in range, one token per logical position
     q = to_device(np.concatenate(qs), cfg.dtype, device) if qs else None
     torch.cuda.synchronize()
     return types.SimpleNamespace(cfg=cfg, pool=pool, batch=batch, q=q, requests=reqs, docs=docs,
