@@ -156,3 +156,129 @@ def test_alibi_attention_bruteforce_and_shift():
             np.testing.assert_allclose(got[i, h], want, rtol=1e-12, atol=1e-12)
     shifted = oracle.attention(q, k, v, qp + 1000, kp + 1000, oracle.AlibiSpec())
     np.testing.assert_allclose(shifted, got, rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------- mutations
+# Each plants a plausible mistake in the oracle's variant code and checks that
+# at least one pin above fails on it.
+
+def _pins():
+    return [test_linear_is_rope_at_interpolated_positions, test_ntk_closed_form,
+            lambda: test_band_limits_and_monotone_blend("yarn", 4096, 1.0, 32.0),
+            lambda: test_band_limits_and_monotone_blend("llama3", 8192, 1.0, 4.0),
+            test_yarn_logit_scale, test_interleaved_pairing_complex_form,
+            test_alibi_slopes_closed_forms, test_alibi_attention_bruteforce_and_shift]
+
+
+def _failing_pins():
+    failed = 0
+    for pin in _pins():
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    return failed
+
+
+def test_every_pin_passes_on_the_oracle():
+    assert _failing_pins() == 0
+
+
+def _freq_mutant(kind, formula):
+    real = RopeSpec.inv_freq
+
+    def inv_freq(self, head_dim):
+        if self.kind != kind:
+            return real(self, head_dim)
+        plain = np.power(self.base, -2.0 * np.arange(head_dim // 2) / head_dim)
+        return formula(self, plain, head_dim)
+    return inv_freq
+
+
+def _yarn_reversed(self, plain, head_dim):
+    r = self.original / (2.0 * np.pi / plain)
+    ramp = np.clip((r - self.low) / (self.high - self.low), 0.0, 1.0)
+    return ramp * plain / self.factor + (1.0 - ramp) * plain
+
+
+def _yarn_no_two_pi(self, plain, head_dim):
+    r = self.original * plain
+    ramp = np.clip((r - self.low) / (self.high - self.low), 0.0, 1.0)
+    return (1.0 - ramp) * plain / self.factor + ramp * plain
+
+
+def _llama3_swapped(self, plain, head_dim):
+    wl = 2.0 * np.pi / plain
+    blend = (self.original / wl - self.low) / (self.high - self.low)
+    mid = (1.0 - blend) * plain / self.factor + blend * plain
+    return np.where(wl < self.original / self.low, plain, np.where(wl > self.original / self.high, plain / self.factor, mid))
+
+
+FREQ_MUTANTS = {
+    "linear multiplies": _freq_mutant("linear", lambda self, p, D: p * self.factor),
+    "ntk exponent D/(D-1)": _freq_mutant(
+        "ntk", lambda self, p, D: np.power(self.base * self.factor ** (D / (D - 1.0)), -2.0 * np.arange(D // 2) / D)),
+    "ntk without exponent": _freq_mutant(
+        "ntk", lambda self, p, D: np.power(self.base * self.factor, -2.0 * np.arange(D // 2) / D)),
+    "yarn ramp reversed": _freq_mutant("yarn", _yarn_reversed),
+    "yarn ratio without 2 pi": _freq_mutant("yarn", _yarn_no_two_pi),
+    "llama3 bands swapped": _freq_mutant("llama3", _llama3_swapped),
+}
+
+
+@pytest.mark.parametrize("name", list(FREQ_MUTANTS))
+def test_frequency_mutants_are_caught(monkeypatch, name):
+    monkeypatch.setattr(RopeSpec, "inv_freq", FREQ_MUTANTS[name])
+    assert _failing_pins() >= 1
+
+
+def test_yarn_temperature_not_squared_is_caught(monkeypatch):
+    def logit_scale(self, head_dim):
+        t = (0.1 * np.log(self.factor) + 1.0) if self.kind == "yarn" and self.factor > 1.0 else 1.0
+        return float(t / np.sqrt(head_dim))
+    monkeypatch.setattr(RopeSpec, "logit_scale", logit_scale)
+    assert _failing_pins() >= 1
+
+
+def test_interleaved_as_half_pairing_is_caught(monkeypatch):
+    import oracle.lazyattn_oracle as lo
+    real = lo.rope
+
+    def rope(x, pos, theta):
+        if isinstance(theta, RopeSpec) and theta.pairing == "interleaved":
+            theta = RopeSpec(theta.base, theta.kind, theta.factor, int(theta.original), theta.low, theta.high)
+        return real(x, pos, theta)
+    monkeypatch.setattr(lo, "rope", rope)
+    monkeypatch.setattr(oracle, "rope", rope)
+    assert _failing_pins() >= 1
+
+
+def test_alibi_mutants_are_caught(monkeypatch):
+    import oracle.lazyattn_oracle as lo
+    real_slopes, real_attn = lo.alibi_slopes, lo.attention_prerotated
+
+    def even_slopes(n):   # the second half from the wrong positions of the 2p sequence
+        p = 1
+        while p * 2 <= n:
+            p *= 2
+        if p == n:
+            return real_slopes(n)
+        geo = [2.0 ** (-8.0 * (i + 1) / (2 * p)) for i in range(2 * p)]
+        return np.array(list(real_slopes(p)) + geo[1::2][: n - p])
+
+    def flipped(q_rot, k_rot, v, q_pos, k_pos, scale=None, alibi=None):
+        return real_attn(q_rot, k_rot, v, q_pos, k_pos, scale, None if alibi is None else -alibi)
+
+    def by_kv_head(q_rot, k_rot, v, q_pos, k_pos, scale=None, alibi=None):
+        if alibi is not None:
+            g = q_rot.shape[1] // k_rot.shape[1]
+            alibi = np.repeat(alibi[::g], g)
+        return real_attn(q_rot, k_rot, v, q_pos, k_pos, scale, alibi)
+
+    for name, target, mutant in (("alibi_slopes", lo, even_slopes), ("attention_prerotated", lo, flipped),
+                                 ("attention_prerotated", lo, by_kv_head)):
+        monkeypatch.setattr(target, name, mutant)
+        if name == "alibi_slopes":
+            monkeypatch.setattr(oracle, "alibi_slopes", mutant)
+        assert _failing_pins() >= 1, mutant.__name__
+        monkeypatch.undo()
