@@ -102,3 +102,38 @@ def test_host_table_check(P):
     assert L.lazyattn_check_batch_host(e, [1, 0], 8, 64) == (L.LAZYATTN_EINVAL, -1)
     with pytest.raises(L.LazyAttnError):
         P.Batch([[P.Segment([0], 0, 10), P.Segment([1], 5, 10)]], device="cpu").check(8, 64)
+
+
+def test_host_table_check_random_tables(P):
+    """Random tables against a direct model: decode every entry, fail on the
+    first request with an out-of-range entry (ERANGE) or a repeated position
+    (EINVAL), range failures taking precedence within a request."""
+    from position_agnostic_kv_lazyattn_gb300 import lazyattn as L
+    rng = np.random.default_rng(61)
+    num_pages, max_position = 40, 300
+    for _ in range(300):
+        R = int(rng.integers(1, 5))
+        ents, offs = [], [0]
+        for _r in range(R):
+            for _e in range(int(rng.integers(0, 6))):
+                ents.append((int(rng.integers(0, 44)), int(rng.integers(0, 300)), int(rng.integers(0, 19)),
+                             int(rng.integers(0, 2))))
+            offs.append(len(ents))
+        packed = P.pack_entries(*zip(*ents)) if ents else np.zeros(0, np.uint64)
+        want = (0, -1)
+        for r in range(R):
+            toks, rc = [], 0
+            for e in packed[offs[r]:offs[r + 1]]:
+                page, start, n, _w = oracle.unpack_entry(int(e))
+                if n == 0:
+                    continue
+                if page >= num_pages or n > 16 or start + n > max_position:
+                    rc = L.LAZYATTN_ERANGE
+                    break
+                toks += range(start, start + n)
+            if rc == 0 and len(set(toks)) != len(toks):
+                rc = L.LAZYATTN_EINVAL
+            if rc:
+                want = (rc, r)
+                break
+        assert L.lazyattn_check_batch_host(packed, offs, num_pages, max_position) == want
