@@ -455,9 +455,11 @@ def reduce_max_over_ranks(local: dict, world: int) -> dict:
     import torch
     import torch.distributed as dist
     keys = sorted(local)
-    t = torch.tensor([float(local[k]) for k in keys], dtype=torch.float64)
+    # NCCL reduces device tensors only; gloo (CPU tests, the reference arm) host ones
+    device = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(local[k]) for k in keys], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return dict(zip(keys, t.tolist()))
+    return dict(zip(keys, t.cpu().tolist()))
 
 
 def cpu_baseline(cfg, budget_s=15.0, n_steps=None):
