@@ -60,6 +60,13 @@ static int host_checks(void) {
     if (lazyattn_pool_create(&d, NULL, &pool) != LAZYATTN_EINVAL || pool) FAIL("zero descriptor accepted");
     if (lazyattn_pool_create(NULL, NULL, &pool) != LAZYATTN_EINVAL) FAIL("NULL descriptor accepted");
     if (lazyattn_store_doc(NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) != LAZYATTN_EINVAL) FAIL("NULL pool");
+    /* block-table check: two requests, the second with two tokens at each of positions 10..12 */
+    uint64_t ent[4] = {lazyattn_pack_entry(0, 0, 16, 0), lazyattn_pack_entry(1, 16, 5, 1),
+                       lazyattn_pack_entry(0, 0, 16, 0), lazyattn_pack_entry(2, 10, 3, 1)};
+    int32_t offs[3] = {0, 2, 4}, bad = 0;
+    if (lazyattn_check_batch_host(ent, offs, 1, 8, 64, &bad) != LAZYATTN_OK || bad != -1) FAIL("valid table");
+    if (lazyattn_check_batch_host(ent, offs, 2, 8, 64, &bad) != LAZYATTN_EINVAL || bad != 1) FAIL("overlap");
+    if (lazyattn_check_batch_host(ent, offs, 2, 2, 64, &bad) != LAZYATTN_ERANGE || bad != 1) FAIL("page range");
     printf("host checks ok\n");
     return 0;
 }
