@@ -30,6 +30,27 @@
  *     and record the first error code in the caller's device status word; they
  *     never trap or hang.
  *   - Not thread-safe per pool: serialise calls that share a pool handle.
+ *   - Entry points that launch work (store_doc, prefill, decode, materialize,
+ *     resolve, decode_noalloc) need the pool's device to be the current one and
+ *     return LAZYATTN_EINVAL, launching nothing, when it is not.
+ *
+ * Input range (bf16 pools)
+ *   The bf16 kernels multiply rotated keys and the rotated, scaled query as
+ *   fp16 operands (fp32 accumulation). A rotation keeps the norm of every
+ *   rotate-half pair (x_i, x_{i+D/2}), so the library accepts any input whose
+ *   pairs satisfy
+ *       keys  : sqrt(k_i^2 + k_{i+D/2}^2)                          <= 65024
+ *       query : sqrt(q_i^2 + q_{i+D/2}^2) * logit_scale * log2(e)  <= 65024
+ *   (logit_scale = 1/sqrt(head_dim), times YaRN's temperature; for head_dim
+ *   128 the query bound is a pair norm of about 509,900). Such pairs stay
+ *   below fp16's maximum (65504) at any angle and through every bf16 rounding
+ *   on the way (materialised or document-local keys). The check runs in fp32 where the values
+ *   enter: keys in lazyattn_store_doc and in the decode append, queries in
+ *   lazyattn_prefill and lazyattn_decode; a pair outside the range (or a NaN)
+ *   records LAZYATTN_ERANGE in the status word, and the outputs that depend on
+ *   it are undefined. V is not checked; its components must stay below 2^90 in
+ *   magnitude for the fp32 accumulators (sums of up to 2^26 keys with weights
+ *   up to 2^8). fp32 pools compute in fp32 and have no such bound.
  *
  * Data layout in device memory (row-major, innermost last)
  *   K pool, V pool : [num_pages][n_kv_heads][16][head_dim], element type dtype,
@@ -155,6 +176,7 @@ typedef struct lazyattn_pool_desc {
 #define LAZYATTN_ROPE_LLAMA3 4
 
 typedef struct lazyattn_pool* lazyattn_pool_t;
+typedef struct lazyattn_plan* lazyattn_plan_t;
 
 /* A batch of requests. Device arrays unless stated otherwise.
  *   num_requests   1 <= R <= 65535 (host value; requests index a grid dimension)
@@ -173,6 +195,11 @@ typedef struct lazyattn_pool* lazyattn_pool_t;
  *                  entry's slot j sits at logical start + j and local start - delta + j;
  *                  0 <= delta <= start. Decode-appended tokens take the local position of
  *                  their slot in the entry they go into.
+ *   decode_plan    lazyattn_decode only (else ignored; may be NULL): a plan built by
+ *                  lazyattn_decode_plan_create from this batch's table and uploaded with
+ *                  lazyattn_decode_plan_upload. With a plan, decode reads each page run that
+ *                  several requests share once per group of requests (see there); without
+ *                  one, every request reads its own pages.
  */
 typedef struct lazyattn_batch {
     int32_t num_requests;
@@ -185,6 +212,7 @@ typedef struct lazyattn_batch {
     const int32_t* q_start;
     int32_t flags;
     const int32_t* entry_delta;
+    lazyattn_plan_t decode_plan;
 } lazyattn_batch;
 
 #define LAZYATTN_OP_PREFILL 0
@@ -206,7 +234,10 @@ uint64_t lazyattn_pack_entry(int32_t page, int32_t start, int32_t nvalid, int32_
 /* Bytes of the position table for head_dim and max_position (host helper). */
 size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position);
 
-/* Create a pool over caller-owned buffers. Validates desc, fills the position
+/* Create a pool over caller-owned buffers (§3 "Problem statement": one store of
+ * documents whose KV is reused at any global offset; §3.1 "Deferred encoding":
+ * the cache holds content only, positions come from the table filled here, as
+ * §3.2 "Prefilling" table-drives cos/sin). Validates desc, fills the position
  * table (fp64 on the host, stored fp32) and zeroes the status word on `stream`,
  * then synchronises that stream before returning. All pages start free.
  * Returns LAZYATTN_OK and *out_pool, or EINVAL/EDTYPE/ECUDA, or ENOSPC when the host
@@ -219,7 +250,9 @@ int lazyattn_pool_destroy(lazyattn_pool_t pool);
 /* Number of free pages (host). */
 int lazyattn_pool_free_count(lazyattn_pool_t pool, int32_t* out_count);
 
-/* Take n free pages (lowest ids first) for caller-managed contents, e.g. the
+/* (§3.2 "Decoding": a request's KV grows by one token per step into pages of
+ * its own, while the shared document pages stay read-only.)
+ * Take n free pages (lowest ids first) for caller-managed contents, e.g. the
  * private pages a request reserves for generated tokens. out_pages: host array
  * of n ids. ENOSPC (nothing taken) if fewer than n are free. */
 int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages);
@@ -229,7 +262,10 @@ int lazyattn_alloc_pages(lazyattn_pool_t pool, int32_t n, int32_t* out_pages);
  * not free pages that queued kernels still read. */
 int lazyattn_free_pages(lazyattn_pool_t pool, const int32_t* pages, int32_t n);
 
-/* Store a document's (or a query segment's) pre-RoPE K/V in fresh pages.
+/* Store a document's (or a query segment's) pre-RoPE K/V in fresh pages
+ * (§3.2: a document's KV is computed once, indexed from position 0, and reused
+ * by every request; §4.3 phase 1, documents are prefilled independently and
+ * cached without positions; §3.1 "Deferred encoding").
  * k, v: device [n_tokens][n_kv_heads][head_dim] in the pool dtype, unrotated.
  * Allocates ceil(n_tokens/16) pages, enqueues the copy on `stream`, writes the
  * page ids (in token order) to the host array out_pages (capacity out_cap) and
@@ -275,6 +311,56 @@ int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const vo
 int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q,
                     const void* k_new, const void* v_new, void* out,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- decode plan
+ * Document-major decode (§3 "Problem statement": requests of one batch read one
+ * document at different global offsets; Fact 3.2: q^T R_{n-m} k depends on
+ * positions only through n - m). A plan groups the pages of a batch's tables
+ * into runs: maximal stretches of consecutive page ids at consecutive logical
+ * positions, cut wherever any request's run starts or ends, so that every
+ * request that reads a run reads all of it, with the same token counts per
+ * page. With the plan, lazyattn_decode gives each run one pass per KV head over
+ * its pages for all the requests that read it (up to 128 query rows, i.e.
+ * 128 / (Hq/Hkv) requests per pass): the keys are rotated once at run-local
+ * positions t, each request's q at m - delta (delta = the request's logical
+ * position of the run's t = 0), and q^T R_{(delta + t) - m} k is the score the
+ * method defines. Each (request, run) pass leaves a partial softmax result that
+ * a combine merges per request. A request's trailing run of writable entries
+ * (its query segment and generated tokens) is its own run, read after the
+ * append. Results equal lazyattn_decode without a plan up to rounding order.
+ *
+ * A plan stays valid while the batch's table changes only by lazyattn_decode's
+ * appends; build a new one after any other change (entries, offsets, pages or
+ * their contents' layout). entries / entry_offsets / entry_delta are HOST copies
+ * of the batch's arrays (entry_delta: doc-local pools only, else NULL).
+ * Host memory only; ENOSPC if it cannot be had; ERANGE / EINVAL for a table
+ * lazyattn_check_batch_host rejects; EDTYPE for fp32 pools (their decode needs no
+ * plan). */
+typedef struct lazyattn_decode_plan_stats {
+    int32_t units;           /* passes per KV head (CTAs per KV head) */
+    int32_t runs;            /* distinct page runs */
+    int32_t partials;        /* partial results per KV head */
+    int32_t max_readers;     /* most (request, occurrence) pairs reading one run */
+    int64_t logical_pages;   /* pages the requests' tables name (with repeats) */
+    int64_t pass_pages;      /* pages the passes read (a run once per pass) */
+} lazyattn_decode_plan_stats;
+
+int lazyattn_decode_plan_create(lazyattn_pool_t pool, const uint64_t* entries, const int32_t* entry_offsets,
+                                const int32_t* entry_delta, int32_t num_requests, lazyattn_plan_t* out_plan);
+
+/* Bytes of device memory the plan's image needs (256-byte aligned buffer). */
+size_t lazyattn_decode_plan_device_bytes(lazyattn_plan_t plan);
+
+/* Copy the plan's image into caller-owned device memory (bytes >= the size
+ * above, 256-byte aligned) on `stream` and remember it; the buffer must stay
+ * valid while batches use the plan. The host image is staged by the runtime
+ * before the call returns. Not for use inside stream capture. */
+int lazyattn_decode_plan_upload(lazyattn_plan_t plan, void* device_buffer, size_t bytes, void* stream);
+
+int lazyattn_decode_plan_get_stats(lazyattn_plan_t plan, lazyattn_decode_plan_stats* out);
+
+/* Release the plan's host memory (its device image stays with the caller). */
+int lazyattn_decode_plan_destroy(lazyattn_plan_t plan);
 
 /* Materialising baseline (what re-encoding systems such as Block-Attention do,
  * §4 "Baselines" and Appendix B): for every entry of `batch`, copy page
@@ -322,12 +408,16 @@ int lazyattn_get_device_status(lazyattn_pool_t pool, int32_t* out_status, int32_
  * fixed array of LAZYATTN_NOALLOC_SCRATCH_BYTES inside the library (device
  * global memory; every GPU that loads the library holds one until the process
  * exits). The call makes no cudaMalloc/cudaFree and no allocating library call.
+ *   - A decode plan in the batch is ignored: this entry point reads each
+ *     request's pages itself (the plan's image would need device memory).
  *   - Returns LAZYATTN_EWORKSPACE, launching nothing, if the batch needs more
  *     scratch than that (lazyattn_workspace_size(pool, LAZYATTN_OP_DECODE, b)
  *     tells how much it needs).
  *   - The pool's device must be current. The first call on a device looks up
- *     the array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *     the array's device address (cudaGetSymbolAddress) and keeps it for the
+ *     life of the process; make that first call before any stream capture, and
+ *     do not use this entry point on a device after cudaDeviceReset (the array
+ *     may then sit elsewhere).
  *   - Every call shares the one array, which keeps the previous call's
  *     contents (the call clears what must start at zero). Calls that overlap
  *     on the GPU - on different streams, or from different threads - race on

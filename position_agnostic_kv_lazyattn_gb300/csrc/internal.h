@@ -94,6 +94,34 @@ __device__ __forceinline__ void record_error(int32_t* status, int32_t code) {
     atomicCAS(status, 0, code);
 }
 
+// Input range of the bf16 kernels (lazyattn.h, "Input range"). Their QK^T MMAs
+// take fp16 operands: a key rotated at any angle, and q rotated and scaled by
+// log2(e) times the logit scale. A rotation keeps the norm of each rotate-half
+// pair (x_i, x_{i+D/2}). With the norm at most 65024 a pair stays finite in
+// fp16 on every path: rotated once (<= 65024); rotated and stored as bf16 (the
+// materialised baseline: each component rounds to at most 65280); or stored
+// rotated as bf16 at document-local positions (the rounding grows the norm by
+// at most 2^-8, to 65278) and rotated again by the document's offset; fp16's
+// largest value is 65504. Checked in fp32 on the values as they arrive; a
+// violation is recorded as LAZYATTN_ERANGE.
+constexpr float kMaxPairNorm = 65024.0f;
+constexpr float kMaxPairNorm2 = kMaxPairNorm * kMaxPairNorm;
+
+// Largest squared pair norm of 8 rotate-half pairs: bf16 x8 of the first half
+// (a) and of the second half (b).
+__device__ __forceinline__ float max_pair_norm2(const uint4& a, const uint4& b) {
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float x0 = __uint_as_float(av[i] << 16), x1 = __uint_as_float(av[i] & 0xffff0000u);
+        const float y0 = __uint_as_float(bv[i] << 16), y1 = __uint_as_float(bv[i] & 0xffff0000u);
+        m = fmaxf(m, fmaxf(fmaf(x0, x0, y0 * y0), fmaf(x1, x1, y1 * y1)));
+        if (!(x0 == x0 && x1 == x1 && y0 == y0 && y1 == y1)) m = INFINITY;   // NaN: out of range too
+    }
+    return m;
+}
+
 // An entry is usable iff its page and every position it covers are in range.
 // Entries failing the check are skipped and reported.
 __device__ __forceinline__ bool entry_ok(const PoolView& pv, uint64_t e) {
@@ -117,7 +145,37 @@ struct DecodeWs {
     int splits;
 };
 
+// ---------------------------------------------------------------- decode plan
+// Device image of a decode plan (lazyattn_decode_plan_create): work units,
+// their users and each request's range of partial results.
+struct PlanUnit {
+    int32_t entry0;    // batch entry of the unit's first page in its first user's table
+    int32_t n_pages;   // pages (entries) of the unit
+    int32_t user0;     // first user of the unit in the users array
+    int32_t n_users;   // users of the unit (bit 31: private tail run, read after the append)
+};
+constexpr int32_t kUnitPrivate = int32_t(1u << 31);
+struct PlanUser {
+    int32_t request;
+    int32_t delta;     // logical position of the unit's run-local position 0 in this request
+    int32_t partial;   // partial-result slot of (this user, this unit)
+    int32_t pad;
+};
+
 }  // namespace lazyattn
+
+struct lazyattn_plan {
+    int32_t num_requests = 0;
+    int32_t num_units = 0;
+    int32_t num_users = 0;
+    int32_t num_partials = 0;
+    int32_t g = 0, hkv = 0;
+    int32_t key_storage = 0;
+    size_t units_off = 0, users_off = 0, pbase_off = 0;
+    std::vector<uint8_t> image;        // the device image, uploaded by lazyattn_decode_plan_upload
+    void* device = nullptr;            // where it was uploaded (caller-owned)
+    lazyattn_decode_plan_stats stats{};
+};
 
 struct lazyattn_pool {
     lazyattn_pool_desc d;
@@ -159,6 +217,13 @@ DecodeWs decode_ws_layout(const lazyattn_pool& p, const lazyattn_batch& b);
 int decode_occupancy(int* ctas_per_sm);
 int launch_decode_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
                        __nv_bfloat16* out, void* ws, const DecodeWs& L, cudaStream_t stream);
+
+// bf16 decode through a plan: document-major units on tcgen05 / TMEM, then a
+// combine of each request's partial results.
+size_t decode_plan_ws_bytes(const lazyattn_pool& p, const lazyattn_plan& plan);
+int decode_shared_init();
+int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const lazyattn_plan& plan,
+                         const __nv_bfloat16* q, __nv_bfloat16* out, void* ws, cudaStream_t stream);
 
 // bf16 prefill on tcgen05 / TMEM with TMA-staged K/V tiles. prefill_init()
 // sets the kernel's shared-memory limit on the current device (done once, at

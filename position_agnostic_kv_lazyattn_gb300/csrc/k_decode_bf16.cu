@@ -291,6 +291,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint32_t qb[8][2];
     uint32_t qx[4][2], qy[4][2];   // LOCAL: q as given (bf16 pairs), rotated per document below
     int last_delta = INT_MIN;
+    bool q_range_ok = true;        // input range: rotated, scaled pairs must stay finite in fp16
+    const float qsc2 = (kLog2e * pv.qk_scale) * (kLog2e * pv.qk_scale);
+    auto check_q = [&](uint32_t x, uint32_t y) {
+        const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
+        const float n2 = fmaxf(fmaf(a0, a0, b0 * b0), fmaf(a1, a1, b1 * b1));
+        q_range_ok = q_range_ok && (n2 * qsc2 <= kMaxPairNorm2);
+    };
     if (LOCAL) {
         const uint32_t* qp = reinterpret_cast<const uint32_t*>(P.q + ((size_t)r * Hq + (size_t)h * g + min(gr, g - 1)) * kD);
 #pragma unroll
@@ -307,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 }
                 qx[t][hf] = x;
                 qy[t][hf] = y;
+                if (gr < g) check_q(x, y);
             }
 #pragma unroll
         for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
@@ -325,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     x = __byte_perm(p0, p1, 0x5410);
                     y = __byte_perm(p0, p1, 0x7632);
                 }
+                check_q(x, y);
                 const float4 cs = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(row + d / 2);
                 const float a0 = bf_lo(x), a1 = bf_hi(x), b0 = bf_lo(y), b1 = bf_hi(y);
                 qb[t][hf] = pack_h2((a0 * cs.x - b0 * cs.y) * sc, (a1 * cs.z - b1 * cs.w) * sc);
@@ -335,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int t = 0; t < 8; ++t) qb[t][0] = qb[t][1] = 0u;
     }
+
+    if (!q_range_ok && s == 0) record_error(pv.status, LAZYATTN_ERANGE);
 
     // ALiBi slopes of this lane's two heads, in the log2 domain of the scores
     const float al0 = ALIBI ? alibi_slope(h * g + min(2 * c, g - 1), Hq) * kLog2e : 0.f;

@@ -30,9 +30,11 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 // Slots past n_tokens in the last page are zero-filled.
 // interleaved (bf16): K rows are de-interleaved on the way (pairs (2i, 2i+1) of
 // an interleaved-RoPE model become the rotate-half pairs (i, i + D/2)).
+// check_range (bf16 pools): every stored key pair must satisfy the input range
+// of the bf16 kernels (max_pair_norm2); a violation is recorded in status.
 __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* kp, uint4* vp,
                                    int32_t n_tokens, int32_t first_page_index, PageList pages, int hkv,
-                                   int row_vecs, int interleaved) {
+                                   int row_vecs, int interleaved, int check_range, int32_t* status) {
     const int j = blockIdx.x;          // page index within this launch
     const int h = blockIdx.y;
     const int32_t page = pages.ids[j];
@@ -47,6 +49,7 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
             if (tok < n_tokens) {
                 const size_t src = ((size_t)tok * hkv + h) * row_vecs + 2 * u;
                 deinterleave16(k[src], k[src + 1], ev, od);
+                if (check_range && max_pair_norm2(ev, od) > kMaxPairNorm2) record_error(status, LAZYATTN_ERANGE);
             }
             kp[dst_base + (size_t)slot * row_vecs + u] = ev;
             kp[dst_base + (size_t)slot * row_vecs + hv + u] = od;
@@ -66,6 +69,9 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
             const size_t src = ((size_t)tok * hkv + h) * row_vecs + c;
             a = k[src];
             b = v[src];
+            // pairs (dims of vector c, dims of vector c + row_vecs / 2)
+            if (check_range && c < row_vecs / 2 && max_pair_norm2(a, k[src + row_vecs / 2]) > kMaxPairNorm2)
+                record_error(status, LAZYATTN_ERANGE);
         }
         kp[dst_base + i] = a;
         vp[dst_base + i] = b;
@@ -78,7 +84,8 @@ __global__ void store_pages_kernel(const uint4* __restrict__ k, const uint4* __r
 // first half) and their rotate-half partners.
 __global__ void store_pages_local_kernel(const __nv_bfloat16* __restrict__ k, const uint4* __restrict__ v,
                                          __nv_bfloat16* kp, uint4* vp, const float2* rope, int32_t n_tokens,
-                                         int32_t first_page_index, PageList pages, int hkv, int D, int interleaved) {
+                                         int32_t first_page_index, PageList pages, int hkv, int D, int interleaved,
+                                         int32_t* status) {
     const int j = blockIdx.x, h = blockIdx.y;
     const int32_t page = pages.ids[j];
     const int tok0 = (first_page_index + j) * kPage;
@@ -102,6 +109,8 @@ __global__ void store_pages_local_kernel(const __nv_bfloat16* __restrict__ k, co
                 *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(src + d);
                 *reinterpret_cast<uint4*>(y) = *reinterpret_cast<const uint4*>(src + d + half);
             }
+            if (max_pair_norm2(*reinterpret_cast<const uint4*>(x), *reinterpret_cast<const uint4*>(y)) > kMaxPairNorm2)
+                record_error(status, LAZYATTN_ERANGE);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const float2 cs = rope[(size_t)tok * half + d + t];
@@ -215,6 +224,7 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
             }
             const uint4 v1 = *reinterpret_cast<const uint4*>(v_new + src + d);
             const uint4 v2 = *reinterpret_cast<const uint4*>(v_new + src + d + half);
+            if (max_pair_norm2(k1, k2) > kMaxPairNorm2) record_error(pv.status, LAZYATTN_ERANGE);
             if (PREROT) {
                 T a[8], b[8];
                 *reinterpret_cast<uint4*>(a) = k1;
@@ -355,12 +365,13 @@ int launch_store_pages(const lazyattn_pool& p, const void* k, const void* v, int
                 static_cast<const __nv_bfloat16*>(k), static_cast<const uint4*>(v),
                 static_cast<__nv_bfloat16*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
                 static_cast<const float2*>(p.d.rope_table), n_tokens, first, pl, p.d.n_kv_heads, p.d.head_dim,
-                p.d.rope_interleaved);
+                p.d.rope_interleaved, p.d.status_word);
         else
             store_pages_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                                                          static_cast<uint4*>(p.d.k_pool), static_cast<uint4*>(p.d.v_pool),
                                                          n_tokens, first, pl, p.d.n_kv_heads, row_vecs,
-                                                         p.d.rope_interleaved);
+                                                         p.d.rope_interleaved, p.d.dtype == LAZYATTN_BF16,
+                                                         p.d.status_word);
         if (cuda_status() != LAZYATTN_OK) return LAZYATTN_ECUDA;
     }
     return LAZYATTN_OK;

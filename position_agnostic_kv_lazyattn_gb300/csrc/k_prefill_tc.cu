@@ -560,6 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (INTER) deinterleave16(a, b, a, b);
                     unpack8(a, x1);
                     unpack8(b, x2);
+                    float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) n2 = fmaxf(n2, fmaf(x1[v], x1[v], x2[v] * x2[v]));
+                    if (!(n2 * sc * sc <= kMaxPairNorm2)) record_error(pv.status, LAZYATTN_ERANGE);
                     const float4* c4 = reinterpret_cast<const float4*>(cs + 16 * u);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {

@@ -32,6 +32,14 @@ lazyattn::PoolView lazyattn_pool::view() const {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launching entry points run on the pool's device only: its buffers and tensor
+// maps belong to that device.
+static int check_device(const lazyattn_pool* pool) {
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return LAZYATTN_ECUDA;
+    return device == pool->device ? LAZYATTN_OK : LAZYATTN_EINVAL;
+}
+
 extern "C" {
 
 const char* lazyattn_status_string(int s) {
@@ -286,7 +294,9 @@ int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32
     const int32_t np = (n_tokens + kPage - 1) / kPage;
     if (out_cap < np) return LAZYATTN_EINVAL;
     if (pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL && n_tokens > pool->d.max_position) return LAZYATTN_EINVAL;
-    int rc = lazyattn_alloc_pages(pool, np, out_pages);
+    int rc = check_device(pool);
+    if (rc != LAZYATTN_OK) return rc;
+    rc = lazyattn_alloc_pages(pool, np, out_pages);
     if (rc != LAZYATTN_OK) return rc;
     rc = launch_store_pages(*pool, k, v, n_tokens, out_pages, np, static_cast<cudaStream_t>(stream));
     if (rc != LAZYATTN_OK) {
@@ -326,6 +336,8 @@ int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const vo
     if (rc != LAZYATTN_OK) return rc;
     if (batch->total_q == 0) return LAZYATTN_OK;
     if (!q || !out || !aligned16(q) || !aligned16(out)) return LAZYATTN_EINVAL;
+    rc = check_device(pool);
+    if (rc != LAZYATTN_OK) return rc;
     (void)workspace;
     (void)workspace_bytes;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -345,6 +357,8 @@ int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const voi
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return LAZYATTN_EINVAL;
     if (workspace_bytes < lazyattn_workspace_size(pool, LAZYATTN_OP_DECODE, batch)) return LAZYATTN_EWORKSPACE;
+    rc = check_device(pool);
+    if (rc != LAZYATTN_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (pool->d.dtype == LAZYATTN_F32) {
         int32_t* qpos = static_cast<int32_t*>(workspace);
@@ -369,6 +383,8 @@ int lazyattn_materialize(lazyattn_pool_t pool, const lazyattn_batch* batch, cons
         pool->d.key_storage == LAZYATTN_KEYS_DOC_LOCAL || pool->d.position_encoding == LAZYATTN_POS_ALIBI)
         return LAZYATTN_EINVAL;
     if (batch->max_entries == 0) return LAZYATTN_OK;
+    rc = check_device(pool);
+    if (rc != LAZYATTN_OK) return rc;
     return launch_materialize(*pool, *batch, dst_entries, static_cast<cudaStream_t>(stream));
 }
 
@@ -377,6 +393,8 @@ int lazyattn_resolve(lazyattn_pool_t pool, const lazyattn_batch* batch, const in
     int rc = check_batch(pool, batch, LAZYATTN_OP_DECODE);
     if (rc != LAZYATTN_OK) return rc;
     if (!out_offsets || !out_triples || out_cap < 0) return LAZYATTN_EINVAL;
+    rc = check_device(pool);
+    if (rc != LAZYATTN_OK) return rc;
     return launch_resolve(*pool, *batch, out_offsets, out_triples, out_cap, static_cast<cudaStream_t>(stream));
 }
 

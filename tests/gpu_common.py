@@ -59,6 +59,37 @@ class Reference:
         steps = [tuple(a[0] for a in workload.decode_inputs(self.cfg, t, [r])) for t in range(n_steps)]
         return oracle.decode_request(self.ctx(r), kq, vq, steps, self.cfg.rope_theta)
 
+    def decode_long(self, r, n_steps):
+        """The same outputs as decode(), for long runs: the oracle's eager form
+        (every key of the request's final sequence rotated once at its logical
+        position by materialize_rotated, then, per step, attention_prerotated
+        over the prefix that ends with the step's own token, q rotated at that
+        token's position). The oracle pins equate the eager and lazy forms."""
+        cfg = self.cfg
+        _, kq, vq = self.qseg(r)
+        steps = [tuple(a[0] for a in workload.decode_inputs(cfg, t, [r])) for t in range(n_steps)]
+        ctx = self.ctx(r)
+        k_all = np.concatenate([k for k, _ in ctx] + [kq] + [s[1][None] for s in steps]).astype(np.float64)
+        v_all = np.concatenate([v for _, v in ctx] + [vq] + [s[2][None] for s in steps]).astype(np.float64)
+        n0 = sum(k.shape[0] for k, _ in ctx) + kq.shape[0]
+        pos = np.arange(k_all.shape[0], dtype=np.int64)
+        k_rot = oracle.materialize_rotated(k_all, pos, cfg.rope_theta)
+        g = cfg.n_q_heads // cfg.n_kv_heads
+        kh = [np.ascontiguousarray(k_rot[:, h, :]) for h in range(cfg.n_kv_heads)]
+        vh = [np.ascontiguousarray(v_all[:, h, :]) for h in range(cfg.n_kv_heads)]
+        scale = oracle.logit_scale(cfg.head_dim, cfg.rope_theta)
+        outs = []
+        for t, (q, _, _) in enumerate(steps):
+            n = n0 + t + 1
+            q_rot = oracle.rope(np.asarray(q, np.float64)[None], np.array([[n - 1]]), cfg.rope_theta)
+            o = np.empty((cfg.n_q_heads, cfg.head_dim))
+            for h in range(cfg.n_kv_heads):
+                o[h * g:(h + 1) * g] = oracle.attention_prerotated(
+                    q_rot[:, h * g:(h + 1) * g], kh[h][:n, None, :], vh[h][:n, None, :], [n - 1],
+                    pos[:n], scale)[0]
+            outs.append(o)
+        return outs
+
 
 def run_decode(L, env, steps, batch=None):
     """`steps` decode calls (append + attention) over env's requests; the

@@ -1,11 +1,20 @@
-"""Host logic of multi-rank runs on CPU (gloo, world size 2): requests are
-sharded as independent replicas with no data-path collective, and a run's
-timing is the max over ranks."""
+"""What bench.py does at N > 1, on CPU (gloo, world size 2).
+
+The path shards as independent replicas: every rank runs the whole workload
+on its own GPU, with no data-path collective. The only cross-rank steps are
+the timing reduction (the slowest rank's time, max over ranks) and the
+whole-job throughput (world x one rank's bytes over that time). The reference
+arm runs on rank 0 alone, which prints the one JSON line; the other ranks exit
+0 without work."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
-import pytest
 import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _free_port():
@@ -17,21 +26,21 @@ def _free_port():
 
 
 def _worker(rank, world, port, q):
-    import sys
-    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    sys.path.insert(0, ROOT)
     import torch.distributed as dist
     import bench
-    import workload
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    shard = workload.shard_requests(130, rank, world)
-    timing = bench.reduce_max_over_ranks({"step_ms": 10.0 + rank, "wall": 1.0 * (2 - rank)}, world)
+    # rank 1 is the slow one for the decode phase, rank 0 for the prefill
+    local = {"dec_s": 0.010 + 0.005 * rank, "pre_ms": 3.0 - rank, "step_ms": 13.0 + 4.0 * rank, "wall": 1.0}
+    timing = bench.reduce_max_over_ranks(local, world)
+    value = bench.replica_throughput(1.0e9, timing["dec_s"], world)
     dist.destroy_process_group()
-    q.put((rank, shard, timing))
+    q.put((rank, timing, value))
 
 
-def test_two_rank_sharding_and_max_timing():
+def test_two_replicas_max_timing_and_whole_job_throughput():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -42,13 +51,33 @@ def test_two_rank_sharding_and_max_timing():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    (_, s0, t0), (_, s1, t1) = res
-    assert s0 + s1 == list(range(130)) and abs(len(s0) - len(s1)) <= 1
-    assert t0 == t1 == {"step_ms": 11.0, "wall": 2.0}
+    (_, t0, v0), (_, t1, v1) = res
+    want = {"dec_s": 0.015, "pre_ms": 3.0, "step_ms": 17.0, "wall": 1.0}
+    for k, v in want.items():
+        assert abs(t0[k] - v) < 1e-12 and abs(t1[k] - v) < 1e-12
+    # 2 replicas x 1 GB each in the slowest rank's 15 ms
+    assert abs(v0 - 2.0e9 / 0.015 / 1e9) < 1e-9 and v0 == v1
 
 
-@pytest.mark.parametrize("n,world", [(16, 1), (16, 3), (5, 8), (0, 2)])
-def test_shard_requests_partition(n, world):
-    import workload
-    got = [workload.shard_requests(n, r, world) for r in range(world)]
-    assert sum(got, []) == list(range(n))
+def test_single_rank_is_unchanged():
+    sys.path.insert(0, ROOT)
+    import bench
+    local = {"dec_s": 0.25, "wall": 2.0}
+    assert bench.reduce_max_over_ranks(local, 1) == local
+    assert abs(bench.replica_throughput(5.0e9, 0.25, 1) - 20.0) < 1e-12
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """bench.py --impl reference launched as the N = 2 runs are (torchrun, one
+    process per rank): rank 0 prints one JSON line, rank 1 prints nothing, both
+    exit 0."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--config", "tiny_fp32"]
+    p = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 2
+    assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0

@@ -276,6 +276,41 @@ def test_hit_ratio_harmonic_special_case():
     assert abs(oracle.hit_ratio_agnostic(100, 100, 0.7) - 1.0) < 1e-15
 
 
+def _harmonic(n, alpha):
+    """sum_{i=1..n} i^-alpha as an exact fraction (alpha in {0, 1, 2})."""
+    from fractions import Fraction
+    return sum((Fraction(1, i ** alpha) for i in range(1, n + 1)), Fraction(0))
+
+
+@pytest.mark.parametrize("C,D,N,alpha", [(4, 2, 10, 1), (5, 2, 10, 1), (7, 3, 10, 1), (9, 4, 12, 2),
+                                         (3, 1, 8, 1), (30, 2, 10, 1), (6, 4, 10, 0), (25, 5, 20, 0)])
+def test_hit_ratios_below_pool_size(C, D, N, alpha):
+    """Eqs. 1 and 2 at C < N (and C // D < N), against exact sums of i^-alpha:
+    Eq. 1 = H(min(C, N)) / H(N); Eq. 2 = H(min(floor(C / D), N)) / H(N). The
+    cases tell floor(C / D) from C / D (5 / 2, 7 / 3, 9 / 4), and the
+    min(., N) bound (30 / 2 = 15 > N = 10); alpha = 0 (uniform popularity)
+    gives the plain coverage fractions min(C, N) / N and floor(C / D) / N."""
+    want_agnostic = _harmonic(min(C, N), alpha) / _harmonic(N, alpha)
+    want_aware = _harmonic(min(C // D, N), alpha) / _harmonic(N, alpha)
+    assert abs(oracle.hit_ratio_agnostic(C, N, float(alpha)) - float(want_agnostic)) < 1e-14
+    assert abs(oracle.hit_ratio_aware(C, D, N, float(alpha)) - float(want_aware)) < 1e-14
+    if alpha == 0:
+        assert abs(oracle.hit_ratio_agnostic(C, N, 0.0) - min(C, N) / N) < 1e-15
+        assert abs(oracle.hit_ratio_aware(C, D, N, 0.0) - (C // D) / N) < 1e-15
+    # Eq. 3 is the ratio of the two (the normaliser cancels), below the pool size
+    if C // D >= 1 and C <= N:
+        assert abs(oracle.hit_ratio_gap(C, D, float(alpha)) -
+                   oracle.hit_ratio_agnostic(C, N, float(alpha)) / oracle.hit_ratio_aware(C, D, N, float(alpha))) < 1e-13
+
+
+def test_hit_ratio_hand_values():
+    """Two values worked by hand: N = 10, alpha = 1, C = 4, D = 2:
+    Eq. 1 = (1 + 1/2 + 1/3 + 1/4) / H_10 = (25/12) / (7381/2520) = 5250/7381,
+    Eq. 2 = (1 + 1/2) / H_10 = 3780/7381."""
+    assert abs(oracle.hit_ratio_agnostic(4, 10, 1.0) - 5250 / 7381) < 1e-15
+    assert abs(oracle.hit_ratio_aware(4, 2, 10, 1.0) - 3780 / 7381) < 1e-15
+
+
 def test_hit_ratio_printed_value():
     """§1 / §2: the printed 2.86x at D = 20, C = 100. The paper omits alpha;
     the gap is monotone in alpha and equals 2.86 (3 digits) near 0.8526."""

@@ -255,11 +255,3 @@ def request_layout(cfg: Config, r: int = 0) -> List[int]:
     """
     lens = doc_lengths(cfg)[request_docs(cfg)[r]]
     return [0] + np.cumsum(lens).astype(np.int64).tolist()
-
-
-def shard_requests(n_requests: int, rank: int, world: int) -> List[int]:
-    """Contiguous block of request indices for one rank (data-parallel replicas)."""
-    base, rem = divmod(n_requests, world)
-    lo = rank * base + min(rank, rem)
-    hi = lo + base + (1 if rank < rem else 0)
-    return list(range(lo, hi))

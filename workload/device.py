@@ -15,6 +15,29 @@ import torch
 from . import Config, PAGE_SIZE, decode_inputs, doc_kv, doc_lengths, query_segment, request_docs, request_layout
 
 
+def _generate_docs(cfg: Config, doc_ids: Sequence[int], window: int = 64):
+    """(doc id, (k, v)) in the order of doc_ids. Documents are drawn by a pool of
+    host threads (each from its own seeded stream, so the values do not depend
+    on the threading), at most `window` ahead of the consumer to bound host
+    memory; pages are still handed out in doc_ids order."""
+    import concurrent.futures
+    import os
+    workers = max(1, min(16, os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        pending = []
+        it = iter(doc_ids)
+        for d in it:
+            pending.append((d, ex.submit(doc_kv, cfg, d)))
+            if len(pending) >= window:
+                break
+        while pending:
+            d, fut = pending.pop(0)
+            nxt = next(it, None)
+            if nxt is not None:
+                pending.append((nxt, ex.submit(doc_kv, cfg, nxt)))
+            yield d, fut.result()
+
+
 def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
     return t if dtype == "f32" else t.to(torch.bfloat16)
@@ -46,10 +69,9 @@ def setup(cfg: Config, requests: Optional[Sequence[int]] = None, baseline: bool 
     pool = DevicePool(num_pages, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.dtype, cfg.rope_theta,
                       cfg.max_position, device, key_storage=key_storage, position_encoding=position_encoding,
                       rope_scaling=rope_scaling, rope_interleaved=rope_interleaved)
-    doc_ids = range(cfg.n_docs) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
+    doc_ids = list(range(cfg.n_docs)) if all_docs else sorted({int(d) for r in reqs for d in docs[r]})
     doc_pages = {}
-    for d in doc_ids:
-        k, v = doc_kv(cfg, d)
+    for d, (k, v) in _generate_docs(cfg, doc_ids):
         doc_pages[d] = pool.store_doc(to_device(k, cfg.dtype, device), to_device(v, cfg.dtype, device))
     segs, qs, q_starts = [], [], []
     for r in reqs:
