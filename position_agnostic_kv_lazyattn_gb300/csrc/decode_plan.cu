@@ -187,7 +187,7 @@ int lazyattn_decode_plan_create(lazyattn_pool_t pool, const uint64_t* E, const i
             u.n_pages = privates[r].second;
             u.order = (int32_t)units.size();
             u.unit = PlanUnit{privates[r].first, privates[r].second, 0, kUnitPrivate};
-            u.users.push_back(PlanUser{r, entry_start(E[privates[r].first]), 0, 0});
+            u.users.push_back(PlanUser{r, user_delta(privates[r].first), 0, 0});
             pass_pages += u.n_pages;
             units.push_back(std::move(u));
         }

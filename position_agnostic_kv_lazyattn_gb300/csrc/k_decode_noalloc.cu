@@ -41,10 +41,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-extern "C" int lazyattn_decode_noalloc(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q,
+extern "C" int lazyattn_decode_noalloc(lazyattn_pool_t pool, const lazyattn_batch* batch_in, const void* q,
                                        const void* k_new, const void* v_new, void* out, void* stream) {
     using namespace lazyattn;
-    if (!pool || !batch) return LAZYATTN_EINVAL;
+    if (!pool || !batch_in) return LAZYATTN_EINVAL;
+    lazyattn_batch batch_copy = *batch_in;
+    batch_copy.decode_plan = nullptr;   // each request reads its own pages (a plan's image needs device memory)
+    const lazyattn_batch* batch = &batch_copy;
     const size_t need = lazyattn_workspace_size(pool, LAZYATTN_OP_DECODE, batch);   // 0: invalid batch
     if (need == 0) return LAZYATTN_EINVAL;
     if (need > (size_t)LAZYATTN_NOALLOC_SCRATCH_BYTES) return LAZYATTN_EWORKSPACE;

@@ -165,7 +165,8 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
         return LAZYATTN_ECUDA;
     }
     int occ = 1;
-    if (d.dtype == LAZYATTN_BF16 && (decode_occupancy(&occ) != LAZYATTN_OK || prefill_init() != LAZYATTN_OK)) {
+    if (d.dtype == LAZYATTN_BF16 && (decode_occupancy(&occ) != LAZYATTN_OK || prefill_init() != LAZYATTN_OK ||
+                                     decode_shared_init() != LAZYATTN_OK)) {
         delete p;
         return LAZYATTN_ECUDA;
     }
@@ -307,6 +308,15 @@ int lazyattn_store_doc(lazyattn_pool_t pool, const void* k, const void* v, int32
     return LAZYATTN_OK;
 }
 
+// A decode plan fits a batch when it was built for its number of requests and
+// the pool's head layout and key storage, and has been uploaded.
+static bool plan_fits(const lazyattn_pool* pool, const lazyattn_batch* b) {
+    const lazyattn_plan* pl = b->decode_plan;
+    return pl->num_requests == b->num_requests && pl->hkv == pool->d.n_kv_heads &&
+           pl->g == pool->d.n_q_heads / pool->d.n_kv_heads && pl->key_storage == pool->d.key_storage &&
+           pl->device != nullptr;
+}
+
 static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int op) {
     if (!pool || !b) return LAZYATTN_EINVAL;
     if (b->num_requests < 1 || b->num_requests > 65535 || b->max_entries < 0 || !b->entries || !b->entry_offsets)
@@ -319,6 +329,8 @@ static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int o
     if (op == LAZYATTN_OP_PREFILL) {
         if (b->total_q < 0 || b->max_q_len < 0 || !b->q_offsets || !b->q_start) return LAZYATTN_EINVAL;
     }
+    if (op == LAZYATTN_OP_DECODE && b->decode_plan && pool->d.dtype == LAZYATTN_BF16 && !plan_fits(pool, b))
+        return LAZYATTN_EINVAL;
     return LAZYATTN_OK;
 }
 
@@ -327,6 +339,7 @@ size_t lazyattn_workspace_size(lazyattn_pool_t pool, int32_t op, const lazyattn_
     if (op == LAZYATTN_OP_PREFILL) return 256;
     if (op != LAZYATTN_OP_DECODE) return 0;
     if (pool->d.dtype == LAZYATTN_F32) return (size_t)batch->num_requests * sizeof(int32_t) + 256;
+    if (batch->decode_plan) return decode_plan_ws_bytes(*pool, *batch->decode_plan);
     return decode_ws_layout(*pool, *batch).total;
 }
 
@@ -366,6 +379,12 @@ int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const voi
         if (rc != LAZYATTN_OK) return rc;
         return launch_attention_f32(*pool, *batch, static_cast<const float*>(q), static_cast<float*>(out),
                                     qpos, st);
+    }
+    if (batch->decode_plan) {   // document-major: qpos at the workspace's start, then the partials
+        rc = launch_decode_append(*pool, *batch, k_new, v_new, static_cast<int32_t*>(workspace), st);
+        if (rc != LAZYATTN_OK) return rc;
+        return launch_decode_shared(*pool, *batch, *batch->decode_plan, static_cast<const __nv_bfloat16*>(q),
+                                    static_cast<__nv_bfloat16*>(out), workspace, st);
     }
     const DecodeWs L = decode_ws_layout(*pool, *batch);
     int32_t* qpos = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.qpos_off);

@@ -66,7 +66,14 @@ class lazyattn_batch(ctypes.Structure):
         ("num_requests", ctypes.c_int32), ("max_entries", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("total_q", ctypes.c_int32), ("entries", ctypes.c_void_p), ("entry_offsets", ctypes.c_void_p),
         ("q_offsets", ctypes.c_void_p), ("q_start", ctypes.c_void_p), ("flags", ctypes.c_int32),
-        ("entry_delta", ctypes.c_void_p),
+        ("entry_delta", ctypes.c_void_p), ("decode_plan", ctypes.c_void_p),
+    ]
+
+
+class lazyattn_decode_plan_stats(ctypes.Structure):
+    _fields_ = [
+        ("units", ctypes.c_int32), ("runs", ctypes.c_int32), ("partials", ctypes.c_int32),
+        ("max_readers", ctypes.c_int32), ("logical_pages", ctypes.c_int64), ("pass_pages", ctypes.c_int64),
     ]
 
 
@@ -95,6 +102,11 @@ def _load():
         "lazyattn_get_device_status": (ctypes.c_int, [vp, P_i32, i32, vp]),
         "lazyattn_decode_noalloc": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_batch), vp, vp, vp, vp, vp]),
         "lazyattn_check_batch_host": (ctypes.c_int, [vp, vp, i32, i32, i32, P_i32]),
+        "lazyattn_decode_plan_create": (ctypes.c_int, [vp, vp, vp, vp, i32, ctypes.POINTER(vp)]),
+        "lazyattn_decode_plan_device_bytes": (sz, [vp]),
+        "lazyattn_decode_plan_upload": (ctypes.c_int, [vp, vp, sz, vp]),
+        "lazyattn_decode_plan_get_stats": (ctypes.c_int, [vp, ctypes.POINTER(lazyattn_decode_plan_stats)]),
+        "lazyattn_decode_plan_destroy": (ctypes.c_int, [vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -109,7 +121,8 @@ EXPORTS = [
     "lazyattn_pool_destroy", "lazyattn_pool_free_count", "lazyattn_alloc_pages", "lazyattn_free_pages",
     "lazyattn_store_doc", "lazyattn_workspace_size", "lazyattn_prefill", "lazyattn_decode",
     "lazyattn_materialize", "lazyattn_resolve", "lazyattn_get_device_status", "lazyattn_decode_noalloc",
-    "lazyattn_check_batch_host",
+    "lazyattn_check_batch_host", "lazyattn_decode_plan_create", "lazyattn_decode_plan_device_bytes",
+    "lazyattn_decode_plan_upload", "lazyattn_decode_plan_get_stats", "lazyattn_decode_plan_destroy",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 LAZYATTN_NOALLOC_SCRATCH_BYTES = NOALLOC_SCRATCH_BYTES
@@ -189,10 +202,46 @@ def lazyattn_store_doc(pool: int, k, v, n_tokens: int, stream=None):
 # --------------------------------------------------------------------- batches
 
 def make_batch(num_requests, max_entries, entries, entry_offsets, q_offsets=None, q_start=None,
-               max_q_len=0, total_q=0, flags=0, entry_delta=None) -> lazyattn_batch:
-    """Fill a lazyattn_batch from device tensors (int64 entries, int32 offsets and deltas)."""
+               max_q_len=0, total_q=0, flags=0, entry_delta=None, decode_plan=None) -> lazyattn_batch:
+    """Fill a lazyattn_batch from device tensors (int64 entries, int32 offsets and deltas)
+    and a decode plan handle (or None)."""
     return lazyattn_batch(num_requests, max_entries, max_q_len, total_q, _ptr(entries), _ptr(entry_offsets),
-                          _ptr(q_offsets), _ptr(q_start), flags, _ptr(entry_delta))
+                          _ptr(q_offsets), _ptr(q_start), flags, _ptr(entry_delta), decode_plan)
+
+
+# --------------------------------------------------------------------- decode plans
+
+def lazyattn_decode_plan_create(pool: int, entries, entry_offsets, entry_delta=None) -> int:
+    """Plan handle for a batch from HOST copies of its table (numpy uint64 entries,
+    int32 offsets [R+1], and int32 document offsets for doc-local pools)."""
+    import numpy as np
+    e = np.ascontiguousarray(entries, dtype=np.uint64)
+    o = np.ascontiguousarray(entry_offsets, dtype=np.int32)
+    d = None if entry_delta is None else np.ascontiguousarray(entry_delta, dtype=np.int32)
+    out = ctypes.c_void_p()
+    _check(lib.lazyattn_decode_plan_create(pool, e.ctypes.data if e.size else None, o.ctypes.data,
+                                           None if d is None else d.ctypes.data, len(o) - 1, ctypes.byref(out)),
+           "lazyattn_decode_plan_create")
+    return out.value
+
+
+def lazyattn_decode_plan_device_bytes(plan: int) -> int:
+    return int(lib.lazyattn_decode_plan_device_bytes(plan))
+
+
+def lazyattn_decode_plan_upload(plan: int, device_buffer, nbytes: int, stream=None):
+    _check(lib.lazyattn_decode_plan_upload(plan, _ptr(device_buffer), nbytes, _stream(stream)),
+           "lazyattn_decode_plan_upload")
+
+
+def lazyattn_decode_plan_get_stats(plan: int) -> dict:
+    st = lazyattn_decode_plan_stats()
+    _check(lib.lazyattn_decode_plan_get_stats(plan, ctypes.byref(st)), "lazyattn_decode_plan_get_stats")
+    return {name: getattr(st, name) for name, _ in lazyattn_decode_plan_stats._fields_}
+
+
+def lazyattn_decode_plan_destroy(plan: int):
+    _check(lib.lazyattn_decode_plan_destroy(plan), "lazyattn_decode_plan_destroy")
 
 
 def lazyattn_check_batch_host(entries, entry_offsets, num_pages: int, max_position: int):

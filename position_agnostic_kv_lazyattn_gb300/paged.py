@@ -152,8 +152,36 @@ class Batch:
             self.q_offsets = self.q_start = None
             self.total_q = self.max_q_len = 0
         self.flags = flags
+        self.plan = None
         self.c = L.make_batch(self.num_requests, self.max_entries, self.entries, self.entry_offsets,
                               self.q_offsets, self.q_start, self.max_q_len, self.total_q, flags, self.entry_delta)
+
+    def plan_decode(self, pool: "DevicePool", stream=None) -> dict:
+        """Build the document-major decode plan of this batch's table
+        (lazyattn_decode_plan_create from the host copy), upload it into a
+        device buffer and make later decode calls through self.c use it.
+        Returns the plan's statistics."""
+        self.drop_plan()
+        delta = self.delta_host if pool.key_storage == "doc_local" else None
+        plan = L.lazyattn_decode_plan_create(pool.handle, self.entries_host, self.offsets_host, delta)
+        nbytes = L.lazyattn_decode_plan_device_bytes(plan)
+        self.plan_buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.entries.device)
+        L.lazyattn_decode_plan_upload(plan, self.plan_buf, nbytes, stream)
+        self.plan = plan
+        self.c.decode_plan = plan
+        return L.lazyattn_decode_plan_get_stats(plan)
+
+    def drop_plan(self):
+        if getattr(self, "plan", None):
+            self.c.decode_plan = None
+            L.lazyattn_decode_plan_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.drop_plan()
+        except Exception:
+            pass
 
     def check(self, num_pages: int, max_position: int):
         """Host check of the table (lazyattn_check_batch_host): entries in range
@@ -167,6 +195,7 @@ class Batch:
         """Same requests and query layout, another entry array (e.g. materialised pages)."""
         b = Batch.__new__(Batch)
         b.__dict__.update(self.__dict__)
+        b.plan = None                      # a plan belongs to one table
         b.entries_host = entries_host.astype(np.uint64)
         b.entries = torch.from_numpy(b.entries_host.view(np.int64).copy()).to(device)
         b.flags = flags

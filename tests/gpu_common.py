@@ -91,13 +91,16 @@ class Reference:
         return outs
 
 
-def run_decode(L, env, steps, batch=None):
+def run_decode(L, env, steps, batch=None, plan=False):
     """`steps` decode calls (append + attention) over env's requests; the
-    outputs of each step, [R][Hq][D] as float arrays."""
+    outputs of each step, [R][Hq][D] as float arrays. plan: decode through the
+    batch's document-major plan (built here)."""
     import torch
     import workload.device  # noqa: F401
     cfg = env.cfg
     batch = batch or env.batch
+    if plan:
+        batch.plan_decode(env.pool)
     nbytes = L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_DECODE, batch.c)
     ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device="cuda")
     out = torch.empty((len(env.requests), cfg.n_q_heads, cfg.head_dim), dtype=env.pool.tdtype, device="cuda")

@@ -7,7 +7,8 @@
   2^8 at a K tile after the first, so prefill must rescale the partial output
   it already holds in TMEM, and decode must rescale in its page loop and merge
   splits whose maxima differ by orders of magnitude. Both key layouts and the
-  materialising baseline, query-head groups of 4 and 8.
+  materialising baseline, query-head groups of 4 and 8, decode with and
+  without a decode plan.
 * The documented input range (lazyattn.h, "Input range"): keys and queries at
   the largest in-range rotate-half pair norms give finite outputs equal to the
   oracle's (the fp16 operands of QK^T would be infinite past fp16's maximum,
@@ -81,9 +82,11 @@ class Request:
         torch.cuda.synchronize()
         return out.float().cpu().numpy(), self.pool.device_status()
 
-    def decode(self, batch=None):
+    def decode(self, batch=None, plan=False):
         L = self.L
         b = batch or self.batch
+        if plan:
+            b.plan_decode(self.pool)
         nbytes = L.lazyattn_workspace_size(self.pool.handle, L.LAZYATTN_OP_DECODE, b.c)
         ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device="cuda")
         outs, status = [], []
@@ -149,9 +152,10 @@ def _score_jump_log2(docs, q, hq, hkv):
     return jump / np.sqrt(D) * np.log2(np.e)
 
 
+@pytest.mark.parametrize("plan", [False, True])
 @pytest.mark.parametrize("hq", [32, 64])
 @pytest.mark.parametrize("keys", ["position_free", "doc_local", "materialised"])
-def test_late_needle_forces_rescale(L, keys, hq):
+def test_late_needle_forces_rescale(L, keys, hq, plan):
     hkv = 8
     docs, q, kq, vq, steps = _needle_inputs(hq, hkv, seed=40 + hq)
     assert _score_jump_log2(docs, q, hq, hkv) > 8.0
@@ -161,7 +165,7 @@ def test_late_needle_forces_rescale(L, keys, hq):
     got, st = req.prefill(batch)
     assert st == 0
     compare(got, oracle.prefill_request(docs, q, kq, vq, THETA), "bf16")
-    outs, sts = req.decode(batch)
+    outs, sts = req.decode(batch, plan=plan)
     assert sts == [0] * len(sts)
     want = oracle.decode_request(docs, kq, vq, steps, THETA)
     for o, w in zip(outs, want):
