@@ -51,6 +51,12 @@
  *   it are undefined. V is not checked; its components must stay below 2^90 in
  *   magnitude for the fp32 accumulators (sums of up to 2^26 keys with weights
  *   up to 2^8). fp32 pools compute in fp32 and have no such bound.
+ *   The kernels read whole pages and give the empty slots of a page (past its
+ *   entry's valid count) zero weight, so those slots must hold finite values:
+ *   lazyattn_store_doc and lazyattn_materialize zero them, and the decode
+ *   append zeroes a page's other slots when it writes the page's first token;
+ *   pages filled by the caller directly must keep them finite too. Pages whose
+ *   entry has no valid slot are not read.
  *
  * Data layout in device memory (row-major, innermost last)
  *   K pool, V pool : [num_pages][n_kv_heads][16][head_dim], element type dtype,

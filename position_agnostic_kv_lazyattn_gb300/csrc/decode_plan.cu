@@ -22,7 +22,8 @@ using namespace lazyattn;
 namespace {
 
 // Longest run one unit walks (pages): longer runs are cut into pieces of this
-// many pages, so that units stay comparable in length.
+// many pages, so that units stay comparable in length (and the kernel's
+// producer warp holds a unit's entries two per lane).
 constexpr int32_t kMaxUnitPages = 64;
 
 struct Reader {
@@ -181,15 +182,17 @@ int lazyattn_decode_plan_create(lazyattn_pool_t pool, const uint64_t* E, const i
             }
         }
         std::stable_sort(units.begin(), units.end(), [](const U& a, const U& b) { return a.n_pages > b.n_pages; });
-        for (int32_t r = 0; r < R; ++r) {
+        for (int32_t r = 0; r < R; ++r) {   // tail runs, in pieces of <= kMaxUnitPages too
             if (privates[r].first < 0) continue;
-            U u;
-            u.n_pages = privates[r].second;
-            u.order = (int32_t)units.size();
-            u.unit = PlanUnit{privates[r].first, privates[r].second, 0, kUnitPrivate};
-            u.users.push_back(PlanUser{r, user_delta(privates[r].first), 0, 0});
-            pass_pages += u.n_pages;
-            units.push_back(std::move(u));
+            for (int32_t k0 = 0; k0 < privates[r].second; k0 += kMaxUnitPages) {
+                U u;
+                u.n_pages = std::min(kMaxUnitPages, privates[r].second - k0);
+                u.order = (int32_t)units.size();
+                u.unit = PlanUnit{privates[r].first + k0, u.n_pages, 0, kUnitPrivate};
+                u.users.push_back(PlanUser{r, user_delta(privates[r].first + k0), 0, 0});
+                pass_pages += u.n_pages;
+                units.push_back(std::move(u));
+            }
         }
 
         // 5. Partial slots: each request's slots are contiguous (pbase[r] ..).

@@ -186,7 +186,8 @@ struct lazyattn_pool {
     int decode_slots = 0;              // resident decode CTAs on the whole GPU
     float qk_scale = 0.f;              // logit scale (1/sqrt(D), YaRN temperature included)
     bool have_maps = false;            // bf16 pools: TMA views of the K and V pools
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap;            // rows of 128 dims, boxes of one page (64 dims x 16 slots)
+    CUtensorMap kmap4, vmap4;          // {D, slot, KV head, page}, boxes of four consecutive pages
     lazyattn::PoolView view() const;
 };
 
@@ -204,8 +205,10 @@ int launch_resolve(const lazyattn_pool& p, const lazyattn_batch& b, const int32_
                    int32_t* out, int32_t cap, cudaStream_t stream);
 
 // TMA views of the bf16 K and V pools as rows of 128 elements (row = (page *
-// Hkv + kv head) * 16 + slot), 64 x 16 boxes, 128-byte swizzle. False if the
-// driver entry point is unavailable or the pool is too large for 32-bit rows.
+// Hkv + kv head) * 16 + slot), 64 x 16 boxes, and as 4-D {D, slot, KV head,
+// page} tensors with boxes of four consecutive pages; 128-byte swizzle. False
+// if the driver entry point is unavailable or the pool is too large for
+// 32-bit rows.
 bool encode_pool_maps(lazyattn_pool& p);
 
 // fp32 SIMT attention (prefill rows or one decode row per request).

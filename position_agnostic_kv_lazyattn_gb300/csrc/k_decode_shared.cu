@@ -13,23 +13,29 @@
 // position n = delta + t. §3.2 "Decoding" (rotate q, not K, per document) is
 // the same move for the paper's own doc-local layout.
 //
-// CTA = (unit u, KV head h): up to 128 query rows, one per (reader, query head
-// of the group). Tiles of 64 keys (4 pages) stream through two-stage K and V
-// rings. Roles (12 warps):
-//   warp 0        TMA producer of K: the unit's entries, each page's
-//                 position-table row for the run-local rotation, tile info
+// CTA = (unit u, KV head h), two per SM: up to 128 query rows, one per
+// (reader, query head of the group), at TMEM lane reader * g + head. Tiles of
+// 64 keys (4 pages) stream through two-stage K and V rings. Roles (12 warps):
+//   warp 0        TMA producer of K: the unit's entries (read by the whole
+//                 warp in one round trip), each page's position-table row for
+//                 the run-local rotation, tile info; four consecutive pages
+//                 with keys are one 4-page box per half of the dims
 //   warp 1        TMEM owner and single-thread UMMA issuer: per tile k,
 //                 S_(k%2) = Q K^T (fp16, M 128 x N 64 x K 128), then, once the
-//                 softmax of tile k is in, O += P_k V (bf16, P from TMEM)
+//                 softmax of tile k is in, O += P_k V (bf16, P from TMEM);
+//                 one commit per QK (K stage free, S ready) and one per PV
+//                 (V stage free, O holds the tile)
 //   warp 2        TMA producer of V
 //   warps 4-7     Q rows (rotated at m - delta, pre-scaled, fp16), softmax of
-//                 each tile (thread = TMEM lane = one row), the partial result
+//                 each tile (thread = TMEM lane = one row; a warp without
+//                 reader rows skips the arithmetic), the partial result
 //   warps 8-11    K rotation in shared memory at run-local positions (fp16),
-//                 zero K and V of empty slots
+//                 zero K of empty slots
 // TMEM (256 columns, two CTAs per SM): S_0, S_1 (64 columns each), O (128);
-// P_k is written as bf16 over the first 32 columns of its S. Rows are spread
-// over the four TMEM lane quarters (row rho at lane (rho % 4) * 32 + rho / 4),
-// so a unit with few readers still has work in every softmax warp.
+// P_k is written as bf16 over the first 32 columns of its S. V needs no
+// fixing up: pages without keys are not read (their rows are outside the
+// tensor maps and read as zeros), and slots past a page's valid count are zero
+// in every page the library fills, so P = 0 meets V = 0 there.
 // Every wait is bounded; a timeout raises an abort flag that all roles honour,
 // drains in-flight copies and MMAs, frees TMEM and records LAZYATTN_EDEVICE.
 #include <limits.h>
@@ -71,6 +77,8 @@ static_assert(2 * kSmemBytes <= 232448, "two CTAs per SM");
 
 struct TileInfo {
     int j;                       // tile index, -1: no more tiles
+    int page0;                   // page of the tile's first entry
+    int consec;                  // pages page0 .. page0 + 3, all with keys: one 4-page box per half
     int rel[kPagesPerTile];      // run-local position of slot 0 of each page (doc-local: relative offset)
     int n[kPagesPerTile];        // keys in each page (0: none / unusable)
     int y[kPagesPerTile];        // row of the page in the K/V tensor maps (out of range: zero fill)
@@ -125,6 +133,26 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// Packed f32x2 arithmetic (two fp32 lanes per instruction).
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "mul.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_neg(float2 a) { return make_float2(-a.x, -a.y); }
 
 __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
     const int n = entry_nvalid(e);
@@ -141,14 +169,17 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_shared_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                         const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4,
                          PoolView pv, SharedParams P) {
     constexpr bool ROT_K = !PREROT && !ALIBI;   // keys rotated here (run-local or relative doc-local)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    __shared__ uint64_t bar_kfull[kStages], bar_kempty[kStages], bar_vfull[kStages], bar_vempty[kStages];
-    __shared__ uint64_t bar_kready[kStages], bar_info[kInfoSlots];
-    __shared__ uint64_t bar_sfull[kStages], bar_pfull[kStages], bar_odone;
+    // qkdone[s]: QK of the tile in stage s is done (its K stage is free and
+    // its S is ready); pvdone[s]: PV of the tile in stage s is done (its V
+    // stage is free, O holds it)
+    __shared__ uint64_t bar_kfull[kStages], bar_qkdone[kStages], bar_vfull[kStages], bar_pvdone[kStages];
+    __shared__ uint64_t bar_kready[kStages], bar_pfull[kStages], bar_info[kInfoSlots];
     __shared__ uint64_t bar_qready, bar_drain;
     __shared__ TileInfo s_info[kInfoSlots];
     __shared__ uint32_t s_tmem;
@@ -161,22 +192,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool priv = (unit.n_users & kUnitPrivate) != 0;
     const int n_users = unit.n_users & ~kUnitPrivate;
     const int np = unit.n_pages;
-    const int T = (np + kPagesPerTile - 1) / kPagesPerTile;
 
     grid_dep_launch_dependents();   // the combine may be scheduled; it waits for this grid
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bar_kfull[s]), 1);
-            mbar_init(smem_u32(&bar_kempty[s]), 1);
+            mbar_init(smem_u32(&bar_qkdone[s]), 1);
             mbar_init(smem_u32(&bar_vfull[s]), 1);
-            mbar_init(smem_u32(&bar_vempty[s]), 1);
+            mbar_init(smem_u32(&bar_pvdone[s]), 1);
             mbar_init(smem_u32(&bar_kready[s]), 4);   // one arrival per rotation warp
-            mbar_init(smem_u32(&bar_sfull[s]), 1);
             mbar_init(smem_u32(&bar_pfull[s]), 4);    // one arrival per softmax warp
         }
         for (int s = 0; s < kInfoSlots; ++s) mbar_init(smem_u32(&bar_info[s]), 1);
-        mbar_init(smem_u32(&bar_odone), 1);
         mbar_init(smem_u32(&bar_qready), 4);
         mbar_init(smem_u32(&bar_drain), 1);
         mbar_fence_init();
@@ -190,83 +218,130 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
+    // waits decided the same way in every lane of a warp (the warp then takes
+    // part in warp-wide TMEM loads and stores together)
+    auto wwait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ K producer
-        // The unit's entries: a shared run's are final before the append runs,
-        // so its copies start at once; a private (tail) run is read after it.
-        // A tile is live iff one of its pages holds keys. The info ring needs no
-        // wait of its own: slot k % 4 last held tile k - 4, whose readers are
-        // all done once QK of tile k - 2 (the K stage wait below) is done.
-        if (lane == 0) {
-            if (priv) grid_dep_wait();
-            const uint64_t* ents = P.entries + unit.entry0;
-            const int32_t* dels = LOCAL ? P.entry_delta + unit.entry0 : nullptr;
-            const uint64_t e0v = ents[0];
-            const int start0 = entry_start(e0v);
-            const int d0 = LOCAL ? dels[0] : 0;
-            int last_k[kStages];
+        // The whole warp reads the unit's entries in one round trip (lane l
+        // holds pages l and l + 32; a unit has at most 64); lane 0 waits on
+        // barriers and issues the copies. A tail run is read after the append;
+        // a shared run's entries and pages are final before it, so its copies
+        // start at once. A K stage is reused once QK of the tile two before is
+        // done. The info ring needs no wait of its own: slot k % 4 last held
+        // tile k - 4, whose readers are all done once QK of tile k - 2 is.
+        if (priv) grid_dep_wait();
+        const uint64_t* ents = P.entries + unit.entry0;
+        uint64_t e[2];
+        int dl[2];
 #pragma unroll
-            for (int s = 0; s < kStages; ++s) last_k[s] = -1;
-            int k = 0;
-            bool ok = true;
-            for (int j = 0; j <= T; ++j) {
-                int n[kPagesPerTile], rel[kPagesPerTile], ys[kPagesPerTile];
-                bool live = false;
+        for (int c = 0; c < 2; ++c) {
+            const int idx = lane + 32 * c;
+            e[c] = idx < np ? ents[idx] : 0ull;
+            dl[c] = (LOCAL && idx < np) ? P.entry_delta[unit.entry0 + idx] : 0;
+        }
+        const int start0 = entry_start(ents[0]);
+        const int d0 = LOCAL ? P.entry_delta[unit.entry0] : 0;
+        int n[2], rel[2];
+        uint32_t pg[2];
+        int jl = -1;
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    const int idx = j * kPagesPerTile + p;
-                    const uint64_t e = (j < T && idx < np) ? ents[idx] : 0ull;
-                    n[p] = usable_tokens(pv, e);
-                    rel[p] = entry_start(e) - start0;
-                    if (LOCAL && n[p] > 0) {
-                        rel[p] = dels[idx] - d0;   // the page's relative rotation
-                        if (rel[p] < 0 || rel[p] >= pv.max_position) n[p] = -1;
-                    }
-                    if (ROT_K && n[p] > 0 && (rel[p] < 0 || rel[p] >= pv.max_position)) n[p] = -1;   // table row
-                    if (n[p] < 0) record_error(pv.status, LAZYATTN_ERANGE);
-                    ys[p] = n[p] > 0 ? ((int)entry_page(e) * Hkv + h) * kPage : P.oob_row;
-                    live = live || n[p] > 0;
-                }
-                if (j < T && !live) continue;
-                const int st = k % kStages;
-                if (k >= kStages && !mbar_wait(smem_u32(&bar_kempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
+        for (int c = 0; c < 2; ++c) {
+            const int idx = lane + 32 * c;
+            pg[c] = entry_page(e[c]);
+            n[c] = idx < np ? usable_tokens(pv, e[c]) : 0;
+            rel[c] = entry_start(e[c]) - start0;
+            if (LOCAL && n[c] > 0) {
+                rel[c] = dl[c] - d0;   // the page's relative rotation
+                if (rel[c] < 0 || rel[c] >= pv.max_position) n[c] = -1;
+            }
+            if (ROT_K && n[c] > 0 && (rel[c] < 0 || rel[c] >= pv.max_position)) n[c] = -1;   // table row
+            if (n[c] < 0) record_error(pv.status, LAZYATTN_ERANGE);
+            if (n[c] > 0) jl = idx / kPagesPerTile;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) jl = max(jl, __shfl_xor_sync(0xffffffffu, jl, off));
+        const int j_last = jl;   // the last tile with keys (-1: none; the unit then has no tile)
+        int last_k[kStages];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) last_k[s] = -1;
+        int k = 0;
+        bool ok = true;
+        for (int j = 0; j <= j_last; ++j) {
+            int tn[kPagesPerTile], trel[kPagesPerTile];
+            uint32_t tpg[kPagesPerTile];
+            bool live = false, consec = true;
+#pragma unroll
+            for (int p = 0; p < kPagesPerTile; ++p) {
+                const int idx = j * kPagesPerTile + p;
+                const int src = idx & 31, c = idx >> 5;
+                tn[p] = __shfl_sync(0xffffffffu, c ? n[1] : n[0], src);
+                trel[p] = __shfl_sync(0xffffffffu, c ? rel[1] : rel[0], src);
+                tpg[p] = __shfl_sync(0xffffffffu, c ? pg[1] : pg[0], src);
+                if (idx >= np) tn[p] = 0;
+                live = live || tn[p] > 0;
+                if (tn[p] <= 0 || tpg[p] != tpg[0] + (uint32_t)p) consec = false;
+            }
+            if (!live) continue;
+            const int st = k % kStages;
+            if (lane == 0) {
+                if (k >= kStages && !mbar_wait(smem_u32(&bar_qkdone[st]), ((k / kStages) - 1) & 1, abort_flag))
                     ok = false;
-                    break;
-                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            if (lane == 0) {
                 TileInfo& info = s_info[k & (kInfoSlots - 1)];
-                const uint32_t ib = smem_u32(&bar_info[k & (kInfoSlots - 1)]);
-                const uint32_t fb = smem_u32(&bar_kfull[st]);
-                if (j == T) {   // sentinel: no more tiles
-                    info.j = -1;
-                    mbar_arrive(ib);
-                    mbar_arrive(fb);
-                    break;
-                }
+                int ys[kPagesPerTile];
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
-                    info.rel[p] = rel[p];
-                    info.n[p] = max(n[p], 0);
+                    ys[p] = tn[p] > 0 ? ((int)tpg[p] * Hkv + h) * kPage : P.oob_row;
+                    info.rel[p] = trel[p];
+                    info.n[p] = max(tn[p], 0);
                     info.y[p] = ys[p];
                 }
                 info.j = j;
-                mbar_arrive(ib);   // releases the info writes to the other roles
+                info.page0 = (int)tpg[0];
+                info.consec = consec ? 1 : 0;
+                mbar_arrive(smem_u32(&bar_info[k & (kInfoSlots - 1)]));   // releases the info writes
+                const uint32_t fb = smem_u32(&bar_kfull[st]);
                 const uint32_t ds = smem_u32(sm + kOffK + st * kKVBytes);
                 const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
                 mbar_arrive_expect_tx(fb, kKVBytes + (ROT_K ? kBaseBytes : 0));
+                if (consec) {
+                    tma_load_4d(ds, &kmap4, 0, 0, h, (int)tpg[0], fb);
+                    tma_load_4d(ds + kKVChunk, &kmap4, 64, 0, h, (int)tpg[0], fb);
+                } else {
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
-                    tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
-                    if (ROT_K) {
-                        const float2* base = pv.rope + (n[p] > 0 ? (size_t)rel[p] * (kD / 2) : 0);
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
+                        tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
+                    }
+                }
+                if (ROT_K) {
+#pragma unroll
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        const float2* base = pv.rope + (tn[p] > 0 ? (size_t)trel[p] * (kD / 2) : 0);
                         bulk_load(bs + p * 512, base, 512, fb);
                     }
                 }
                 last_k[st] = k;
-                ++k;
             }
-            if (!ok) *abort_flag = 1;
+            ++k;
+        }
+        if (lane == 0) {
+            const int st = k % kStages;
+            if (ok && (k < kStages ||
+                       mbar_wait(smem_u32(&bar_qkdone[st]), ((k / kStages) - 1) & 1, abort_flag))) {
+                s_info[k & (kInfoSlots - 1)].j = -1;   // sentinel: no more tiles
+                mbar_arrive(smem_u32(&bar_info[k & (kInfoSlots - 1)]));
+                mbar_arrive(smem_u32(&bar_kfull[st]));
+            } else {
+                *abort_flag = 1;
+            }
             if (*abort_flag) {   // let issued copies land before the CTA's smem is released
                 volatile int never = 0;
                 for (int s = 0; s < kStages; ++s)
@@ -290,17 +365,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 int ys[kPagesPerTile];
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) ys[p] = info.y[p];
-                if (k >= kStages && !mbar_wait(smem_u32(&bar_vempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
+                const int consec = info.consec, page0 = info.page0;
+                if (k >= kStages && !mbar_wait(smem_u32(&bar_pvdone[st]), ((k / kStages) - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&bar_vfull[st]);
                 const uint32_t ds = smem_u32(sm + kOffV + st * kKVBytes);
                 mbar_arrive_expect_tx(fb, kKVBytes);
+                if (consec) {
+                    tma_load_4d(ds, &vmap4, 0, 0, h, page0, fb);
+                    tma_load_4d(ds + kKVChunk, &vmap4, 64, 0, h, page0, fb);
+                } else {
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
-                    tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
+                        tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                    }
                 }
                 last_k[st] = k;
             }
@@ -333,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint64_t ob = (uint64_t)(((t >> 2) * kKVChunk + (t & 3) * 32) >> 4);
                     umma_f16(d, dq0 + oa, b0 + ob, idqk, t > 0 ? 1u : 0u);
                 }
-                umma_commit(smem_u32(&bar_sfull[st]));
-                umma_commit(smem_u32(&bar_kempty[st]));   // K stage free once these MMAs finish
+                umma_commit(smem_u32(&bar_qkdone[st]));   // S ready, K stage free
             };
             // O += P_k V_k: P_k (bf16, 128 rows x 64 keys) is the first 32 columns of S_(k%2).
             auto issue_pv = [&](int k) {
@@ -344,8 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int t = 0; t < kN / 16; ++t)
                     umma_f16_ts(tmem + kColO, a + 8 * t, b0 + (uint64_t)(t * 128), idpv, (t > 0 || k > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_odone));
-                umma_commit(smem_u32(&bar_vempty[st]));
+                umma_commit(smem_u32(&bar_pvdone[st]));   // O holds the tile, V stage free
             };
             auto kready = [&](int k) {
                 return mbar_wait(smem_u32(&bar_kready[k % kStages]), (k / kStages) & 1, abort_flag);
@@ -379,18 +458,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ------------------------------------------------------------ K rotation
         // Thread = (slot, group u of 8 frequencies): dims 8u..8u+7 of the first
         // half and 64+8u.. of the second half of every key row with this slot.
+        // The angle of slot s of a page is the page's row (cos, sin)(rel theta)
+        // composed with (cos, sin)(s theta) (doc-local: the page's row alone).
         const int rt = threadIdx.x - 256;
         const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
-        float cs[8], sn[8];   // (cos, sin)(slot * theta_f), f = 8u + 0..7
+        float2 cs2[4], sn2[4];   // (cos, sin)(slot * theta_f) for f = 8u + 2v, 8u + 2v + 1
         if (ROT_K && !LOCAL) {
             const float4* t4 = reinterpret_cast<const float4*>(pv.rope + (size_t)slot * (kD / 2) + 8 * u);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
-                cs[2 * v] = f.x;
-                sn[2 * v] = f.y;
-                cs[2 * v + 1] = f.z;
-                sn[2 * v + 1] = f.w;
+                cs2[v] = make_float2(f.x, f.z);
+                sn2[v] = make_float2(f.y, f.w);
             }
         }
         // One thread polls the stage's barrier; the named barrier releases the
@@ -418,14 +497,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             int n[kPagesPerTile];
-            bool partial = false;
 #pragma unroll
-            for (int p = 0; p < kPagesPerTile; ++p) {
-                n[p] = info.n[p];
-                partial = partial || n[p] < kPage;
-            }
+            for (int p = 0; p < kPagesPerTile; ++p) n[p] = info.n[p];
             uint8_t* kb = sm + kOffK + st * kKVBytes;
-            uint8_t* vb = sm + kOffV + st * kKVBytes;
             const uint8_t* bb = sm + kOffBase + st * kBaseBytes + u * 64;
 #pragma unroll 2
             for (int p = 0; p < kPagesPerTile; ++p) {
@@ -439,18 +513,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (ROT_K) {
                         const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float4 b = b4[v];
-#pragma unroll
-                            for (int w = 0; w < 2; ++w) {
-                                const int f = 2 * v + w;
-                                const float cb = w ? b.z : b.x, sb = w ? b.w : b.y;
-                                const float c = LOCAL ? cb : cb * cs[f] - sb * sn[f];
-                                const float s = LOCAL ? sb : sb * cs[f] + cb * sn[f];
-                                const float a = x1[f], z = x2[f];
-                                x1[f] = a * c - z * s;
-                                x2[f] = a * s + z * c;
+                        for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1
+                            const float4 bv = b4[v];
+                            float2 c = make_float2(bv.x, bv.z), s = make_float2(bv.y, bv.w);
+                            if (!LOCAL) {   // angle of rel + slot
+                                const float2 cc = f2_fma(c, cs2[v], f2_mul(f2_neg(s), sn2[v]));
+                                s = f2_fma(s, cs2[v], f2_mul(c, sn2[v]));
+                                c = cc;
                             }
+                            const float2 a = make_float2(x1[2 * v], x1[2 * v + 1]);
+                            const float2 z = make_float2(x2[2 * v], x2[2 * v + 1]);
+                            const float2 r1 = f2_fma(a, c, f2_mul(f2_neg(z), s));
+                            const float2 r2 = f2_fma(a, s, f2_mul(z, c));
+                            x1[2 * v] = r1.x;
+                            x1[2 * v + 1] = r1.y;
+                            x2[2 * v] = r2.x;
+                            x2[2 * v + 1] = r2.y;
                         }
                     }
                     *p1 = pack8_h(x1);
@@ -458,16 +536,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 } else {   // no key in this slot: zero K so that its scores stay finite
                     *p1 = make_uint4(0, 0, 0, 0);
                     *p2 = make_uint4(0, 0, 0, 0);
-                }
-            }
-            if (partial) {   // empty slots: zero V too (0 * NaN would be NaN)
-                if (!rot_wait(smem_u32(&bar_vfull[st]), ph)) break;
-#pragma unroll 1
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    if (slot < n[p]) continue;
-                    const int kr = p * kPage + slot;
-                    *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
@@ -478,8 +546,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ------------------------------------------------------------ rows: Q, softmax, partials
         const int quarter = warp - 4;
         const int trow = 32 * quarter + lane;      // TMEM lane = row of the Q tile
-        const int rho = lane * 4 + quarter;        // (reader, head) index of the row
-        const int j = rho / g, head = rho - j * g;
+        const int j = trow / g, head = trow - j * g;
         const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
         const bool reader = j < n_users;
         PlanUser us = {0, 0, 0, 0};
@@ -492,53 +559,47 @@ __global__ void __launch_bounds__(kThreads, 2)
             record_error(pv.status, LAZYATTN_ERANGE);
             row_valid = false;
         }
-        {
+        // a warp without a row that takes part skips the arithmetic (not the barriers)
+        const bool active = __any_sync(0xffffffffu, row_valid);
+        if (row_valid) {
             uint8_t* qsm = sm + kOffQ;
             const float sc = kLog2e * pv.qk_scale;
             const __nv_bfloat16* qp_ = P.q + ((size_t)us.request * Hq + (size_t)h * g + head) * kD;
-            const float* csq = reinterpret_cast<const float*>(pv.rope + (size_t)(row_valid ? pos_q : 0) * (kD / 2));
+            const float* csq = reinterpret_cast<const float*>(pv.rope + (size_t)pos_q * (kD / 2));
+            float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
 #pragma unroll 2
             for (int uu = 0; uu < 8; ++uu) {
-                uint4 w1 = make_uint4(0, 0, 0, 0), w2 = w1;
-                if (row_valid) {
-                    float x1[8], x2[8];
-                    uint4 a = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * uu : 8 * uu)));
-                    uint4 b = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * uu + 8 : 64 + 8 * uu)));
-                    if (INTER) deinterleave16(a, b, a, b);
-                    unpack8(a, x1);
-                    unpack8(b, x2);
-                    float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
+                float x1[8], x2[8];
+                uint4 a = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * uu : 8 * uu)));
+                uint4 b = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * uu + 8 : 64 + 8 * uu)));
+                if (INTER) deinterleave16(a, b, a, b);
+                unpack8(a, x1);
+                unpack8(b, x2);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) n2 = fmaxf(n2, fmaf(x1[v], x1[v], x2[v] * x2[v]));
-                    if (!(n2 * sc * sc <= kMaxPairNorm2)) record_error(pv.status, LAZYATTN_ERANGE);
-                    const float4* c4 = reinterpret_cast<const float4*>(csq + 16 * uu);
+                for (int v = 0; v < 8; ++v) n2 = fmaxf(n2, fmaf(x1[v], x1[v], x2[v] * x2[v]));
+                const float4* c4 = reinterpret_cast<const float4*>(csq + 16 * uu);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const float4 f = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(c4 + v);
-                        const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
-                        x1[2 * v] = (a0 * f.x - z0 * f.y) * sc;
-                        x2[2 * v] = (a0 * f.y + z0 * f.x) * sc;
-                        x1[2 * v + 1] = (a1 * f.z - z1 * f.w) * sc;
-                        x2[2 * v + 1] = (a1 * f.w + z1 * f.z) * sc;
-                    }
-                    w1 = pack8_h(x1);
-                    w2 = pack8_h(x2);
+                for (int v = 0; v < 4; ++v) {
+                    const float4 f = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(c4 + v);
+                    const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
+                    x1[2 * v] = (a0 * f.x - z0 * f.y) * sc;
+                    x2[2 * v] = (a0 * f.y + z0 * f.x) * sc;
+                    x1[2 * v + 1] = (a1 * f.z - z1 * f.w) * sc;
+                    x2[2 * v + 1] = (a1 * f.w + z1 * f.z) * sc;
                 }
-                *reinterpret_cast<uint4*>(qsm + sw128_offset(trow, uu)) = w1;
-                *reinterpret_cast<uint4*>(qsm + kQChunk + sw128_offset(trow, uu)) = w2;
+                *reinterpret_cast<uint4*>(qsm + sw128_offset(trow, uu)) = pack8_h(x1);
+                *reinterpret_cast<uint4*>(qsm + kQChunk + sw128_offset(trow, uu)) = pack8_h(x2);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bar_qready));
+            if (!(n2 * sc * sc <= kMaxPairNorm2)) record_error(pv.status, LAZYATTN_ERANGE);
         }
+        // Rows past the readers keep whatever the Q buffer held: their scores
+        // and outputs are never used (each row of an MMA is independent).
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_qready));
         // ALiBi: slope of this row's query head, in the log2 domain of the scores
         const float alibi_c1 = ALIBI ? alibi_slope(h * g + head, Hq) * kLog2e : 0.f;
 
-        // waits decided the same way in every lane (the warp then takes part in
-        // warp-wide TMEM loads and stores together)
-        auto wwait = [&](uint32_t bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
-        };
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int k = 0;
@@ -555,92 +616,99 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int l0 = info.n[2 * w], l1 = info.n[2 * w + 1];
                 vis[w] = ((1u << l0) - 1u) | (((1u << l1) - 1u) << 16);
             }
+            int rel[kPagesPerTile];
+#pragma unroll
+            for (int p = 0; p < kPagesPerTile; ++p) rel[p] = info.rel[p];
             const bool wfull = (vis[0] & vis[1]) == 0xffffffffu;   // same for every row of the CTA
             const int st = k % kStages;
-            ok = wwait(smem_u32(&bar_sfull[st]), (k / kStages) & 1);
+            ok = wwait(smem_u32(&bar_qkdone[st]), (k / kStages) & 1);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t ts = tl + (uint32_t)(st * kN);
-            // ALiBi (log2 domain): key i of page q gets alibi_c1 * (rel_q + i - pos_q)
-            auto page_delta = [&](int q) { return info.rel[q] - pos_q; };
-            float mx = -INFINITY;
+            if (active) {
+                const uint32_t ts = tl + (uint32_t)(st * kN);
+                // ALiBi (log2 domain): key i of page q gets alibi_c1 * (rel_q + i - pos_q)
+                auto page_delta = [&](int q) { return rel[q] - pos_q; };
+                // two passes over the row's 64 scores, 32 columns at a time (the
+                // registers of two CTAs per SM do not hold all 64 at once)
+                float mx = -INFINITY;   // the row maximum (ALiBi: an upper bound of the biased scores)
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {   // pass 1: the row maximum (ALiBi: an upper bound)
-                uint32_t v[32];
-                tmem_ld32(ts + 32 * hh, v);
-                if (!wfull) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = (vis[hh] >> i) & 1u ? v[i] : 0xff800000u;
-                }
-                if (ALIBI) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        float a = -INFINITY;
-#pragma unroll
-                        for (int i = 0; i < 16; i += 2)
-                            a = fmax3(a, __uint_as_float(v[16 * q + i]), __uint_as_float(v[16 * q + i + 1]));
-                        mx = fmaxf(mx, a + alibi_c1 * (float)min(page_delta(2 * hh + q) + 15, 0));
-                    }
-                } else {
-                    float a = -INFINITY, b = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        a = fmax3(a, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        b = fmax3(b, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                    }
-                    mx = fmax3(mx, a, b);
-                }
-            }
-            float alpha = 1.f;
-            if (mx > m_run + kRescaleThreshold) {
-                alpha = fast_exp2(m_run - mx);   // 0 when m_run is -inf
-                m_run = mx;
-            }
-            const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-            // O holds tiles < k once PV of tile k - 1 is done; rescale it when
-            // the reference maximum moved for some row of the warp. (S of tile
-            // k is done, so PV of tile k - 2, issued before QK of tile k, is
-            // done: odone is at most one phase behind and the parity wait holds.)
-            if (k >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = wwait(smem_u32(&bar_odone), (k - 1) & 1);
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int hh = 0; hh < 2; ++hh) {
                     uint32_t v[32];
-                    tmem_ld32(tl + kColO + 32 * c, v);
+                    tmem_ld32(ts + 32 * hh, v);
+                    if (!wfull) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(tl + kColO + 32 * c, v);
-                }
-            }
-            // pass 2: P = 2^(s - mref) as bf16 pairs over S's first 32 columns
-            float sum = 0.f;
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                tmem_ld32(ts + 32 * hh, v);
-                if (!wfull) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = (vis[hh] >> i) & 1u ? v[i] : 0xff800000u;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float e0 = __uint_as_float(v[2 * i]) - mref, e1 = __uint_as_float(v[2 * i + 1]) - mref;
-                    if (ALIBI) {
-                        const float b0 = alibi_c1 * (float)(page_delta(2 * hh + (i >> 3)) + 2 * (i & 7));
-                        e0 += b0;
-                        e1 += b0 + alibi_c1;
+                        for (int i = 0; i < 32; ++i) v[i] = (vis[hh] >> i) & 1u ? v[i] : 0xff800000u;
                     }
-                    const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
-                    sum += p0 + p1;
-                    pk[i] = pack_bf2(p0, p1);
+                    if (ALIBI) {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            float a = -INFINITY;
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2)
+                                a = fmax3(a, __uint_as_float(v[16 * q + i]), __uint_as_float(v[16 * q + i + 1]));
+                            mx = fmaxf(mx, a + alibi_c1 * (float)min(page_delta(2 * hh + q) + 15, 0));
+                        }
+                    } else {
+                        float a = -INFINITY, c = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            a = fmax3(a, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                            c = fmax3(c, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        }
+                        mx = fmax3(mx, a, c);
+                    }
                 }
-                tmem_st16(ts + 16 * hh, pk);
+                float alpha = 1.f;
+                if (mx > m_run + kRescaleThreshold) {
+                    alpha = fast_exp2(m_run - mx);   // 0 when m_run is -inf
+                    m_run = mx;
+                }
+                const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+                // O holds tiles < k once PV of tile k - 1 is done; rescale it when
+                // the reference maximum moved for some row of the warp. (S of tile
+                // k is done, so PV of tile k - 2, issued before QK of tile k, is
+                // done: pvdone[(k-1)%2] is at most one phase behind.)
+                if (k >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    ok = wwait(smem_u32(&bar_pvdone[(k - 1) % kStages]), ((k - 1) / kStages) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + kColO + 32 * c, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tl + kColO + 32 * c, o);
+                    }
+                }
+                // P = 2^(s - mref) as bf16 pairs over S's first 32 columns
+                float sum = 0.f;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[32];
+                    tmem_ld32(ts + 32 * hh, v);
+                    if (!wfull) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = (vis[hh] >> i) & 1u ? v[i] : 0xff800000u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float e0 = __uint_as_float(v[2 * i]) - mref, e1 = __uint_as_float(v[2 * i + 1]) - mref;
+                        if (ALIBI) {
+                            const float b0 = alibi_c1 * (float)(page_delta(2 * hh + (i >> 3)) + 2 * (i & 7));
+                            e0 += b0;
+                            e1 += b0 + alibi_c1;
+                        }
+                        const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+                        sum += p0 + p1;
+                        pk[i] = pack_bf2(p0, p1);
+                    }
+                    tmem_st16(ts + 16 * hh, pk);
+                }
+                l_run = l_run * alpha + sum;
+                tmem_wait_st();
             }
-            l_run = l_run * alpha + sum;
-            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_pfull[st]));
@@ -648,10 +716,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // partial result of the row: O (unnormalised), its reference maximum and sum.
         // O is final once every MMA is: the issuer commits the drain barrier
-        // (single phase) after the last PV. (Waiting on odone's last phase would
-        // not do: QK of tile K-1 is issued before PV of tile K-2, so when the
-        // last softmax ends only PV of tile K-3 is known to be done, and a
-        // parity wait two phases behind returns at once.)
+        // (single phase) after the last PV. (Waiting on the last PV's own
+        // barrier phase would not do: QK of tile K-1 is issued before PV of
+        // tile K-2, so when the last softmax ends only PV of tile K-3 is known
+        // to be done, and a parity wait two phases behind returns at once.)
         if (ok && k >= 1) ok = wwait(smem_u32(&bar_drain), 0);
         tc_fence_after();
         const bool have = ok && k >= 1 && row_valid && l_run > 0.f;
@@ -664,13 +732,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             float4* dst = reinterpret_cast<float4*>(P.acc + (((size_t)us.partial * Hkv + h) * g + head) * kD);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + kColO + 32 * c, v);
+                uint32_t o[32];
+                tmem_ld32(tl + kColO + 32 * c, o);
                 if (have) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        dst[8 * c + i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                        dst[8 * c + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                                     __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
                 }
             }
         }
@@ -727,7 +795,8 @@ __global__ void __launch_bounds__(128)
                       pack_bf2(a[4] * inv, a[5] * inv), pack_bf2(a[6] * inv, a[7] * inv));
 }
 
-using SharedKernel = void (*)(const CUtensorMap, const CUtensorMap, PoolView, SharedParams);
+using SharedKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, PoolView,
+                              SharedParams);
 
 SharedKernel shared_kernel_for(bool prerot, bool local, bool inter, bool alibi) {
     if (alibi) return decode_shared_kernel<false, false, false, true>;
@@ -787,7 +856,8 @@ int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const 
                                   p.d.rope_interleaved != 0, p.d.position_encoding == LAZYATTN_POS_ALIBI);
     if (plan.num_units > 0) {
         dim3 grid(plan.num_units, p.d.n_kv_heads);
-        if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.view(), P) !=
+        if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.kmap4, p.vmap4, p.view(),
+                             P) !=
             cudaSuccess)
             return LAZYATTN_ECUDA;
     }

@@ -205,6 +205,21 @@ __global__ void decode_append_kernel(PoolView pv, uint64_t* entries, const int32
     const int D = pv.d, half = D / 2;
     T* kp = static_cast<T*>(pv.k_pool);
     T* vp = static_cast<T*>(pv.v_pool);
+    if (slot == 0) {
+        // The first token into a page: its other slots (whatever the page held
+        // before) become zeros, so that slots past a page's valid count are
+        // zero in every page the library fills (the attention kernels read
+        // whole pages and only mask the scores of empty slots).
+        const int row = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
+        uint4* k4 = reinterpret_cast<uint4*>(kp);
+        uint4* v4 = reinterpret_cast<uint4*>(vp);
+        for (int i = threadIdx.x; i < pv.hkv * (kPage - 1) * row; i += blockDim.x) {
+            const int h = i / ((kPage - 1) * row), rest = i % ((kPage - 1) * row);
+            const size_t at = ((((size_t)page * pv.hkv + h) * kPage) + 1) * row + rest;
+            k4[at] = make_uint4(0, 0, 0, 0);
+            v4[at] = make_uint4(0, 0, 0, 0);
+        }
+    }
     if (sizeof(T) == 2 && half % 8 == 0) {
         // 16-byte vectors: thread = (kv head, 8 dims of the first half) and
         // their rotate-half partners; rows are 16-byte aligned (D % 16 == 0,

@@ -453,10 +453,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One thread polls the stage's barrier and a named barrier releases the
         // other 127: every mbarrier update (each TMA copy's bytes) wakes its
         // pollers, and 128 pollers would take issue slots from the math roles.
+        // The named barrier also makes the go / no-go decision the same for all
+        // 128 threads (each reading the abort flag on its own could split them).
         auto rot_wait = [&](uint32_t bar, uint32_t parity) {
-            if (rt == 0) mbar_wait(bar, parity, abort_flag);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            return *abort_flag == 0;
+            int go = 1;
+            if (rt == 0) go = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+            go = go && *abort_flag == 0;
+            int all;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+                "selp.b32 %0, 1, 0, q;\n\t}"
+                : "=r"(all)
+                : "r"(go)
+                : "memory");
+            return all != 0;
         };
         for (int k = 0; T > 0; ++k) {
             const int st = k % kStages, ph = (k / kStages) & 1;
@@ -468,14 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             int n[kPagesPerTile];
-            bool partial = false;   // a page with some, but not all, slots holding keys
 #pragma unroll
-            for (int p = 0; p < kPagesPerTile; ++p) {
-                n[p] = info.n[p];
-                partial = partial || (n[p] > 0 && n[p] < kPage);
-            }
+            for (int p = 0; p < kPagesPerTile; ++p) n[p] = info.n[p];
             uint8_t* kb = sm + kOffK + st * kKVBytes;
-            uint8_t* vb = sm + kOffV + st * kKVBytes;
             const uint8_t* bb = sm + kOffBase + st * kBaseBytes + u * 64;
 #pragma unroll 2
             for (int p = 0; p < kPagesPerTile; ++p) {
@@ -511,16 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *p2 = make_uint4(0, 0, 0, 0);
                 }
             }
-            if (partial) {   // stale slots of a partly filled page: zero V too (0 * NaN would be NaN)
-                if (!rot_wait(smem_u32(&bar_vfull[st]), ph)) break;
-#pragma unroll 1
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    if (slot < n[p]) continue;
-                    const int kr = p * kPage + slot;
-                    *reinterpret_cast<uint4*>(vb + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(vb + kKVChunk + sw128_offset(kr, u)) = make_uint4(0, 0, 0, 0);
-                }
-            }
+            // V needs no work here: pages without keys are not read (their rows
+            // are outside the tensor map and read as zeros), and slots past a
+            // page's valid count are zero in every page the library fills, so
+            // P = 0 meets V = 0 there.
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_kready[st]));

@@ -31,6 +31,20 @@ bool encode_one(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same pool as a 4-D tensor {D, slot, KV head, page} (strides 2 B, D * 2 B,
+// 16 * D * 2 B, Hkv * 16 * D * 2 B) with boxes {64, 16, 1, 4}: one box holds
+// half the dims of four consecutive pages of one KV head, rows ordered
+// (page, slot) exactly as four 2-D page boxes side by side.
+bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t pages, int hkv, int d) {
+    cuuint64_t gdim[4] = {(cuuint64_t)d, (cuuint64_t)kPage, (cuuint64_t)hkv, (cuuint64_t)pages};
+    cuuint64_t gstride[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * kPage, (cuuint64_t)d * 2 * kPage * hkv};
+    cuuint32_t box[4] = {64, (cuuint32_t)kPage, 1, 4};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool encode_pool_maps(lazyattn_pool& p) {
@@ -42,6 +56,8 @@ bool encode_pool_maps(lazyattn_pool& p) {
     if (!enc) return false;
     if (!encode_one(enc, &p.kmap, p.d.k_pool, rows, p.d.head_dim)) return false;
     if (!encode_one(enc, &p.vmap, p.d.v_pool, rows, p.d.head_dim)) return false;
+    if (!encode_run(enc, &p.kmap4, p.d.k_pool, (uint64_t)p.d.num_pages, p.d.n_kv_heads, p.d.head_dim)) return false;
+    if (!encode_run(enc, &p.vmap4, p.d.v_pool, (uint64_t)p.d.num_pages, p.d.n_kv_heads, p.d.head_dim)) return false;
     p.have_maps = true;
     return true;
 }
