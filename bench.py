@@ -50,12 +50,13 @@ def peaks():
 
 
 # DRAM bytes (read + write) per launch from one ncu capture of this bench's own
-# command on the named workload (summary: profiles/traffic_llama3_8b.md), keyed
+# command on the named workload (summary: profiles/traffic_llama3_70b.md), keyed
 # by a hash of the kernel sources the capture ran; reported only while the
 # sources still hash the same, else null. "decode" = one lazyattn_decode call
-# (append + attention kernels), "prefill" = the prefill kernel.
+# through the batch's decode plan (append + document-major units + combine),
+# "prefill" = the prefill kernel.
 KERNEL_SOURCES = {
-    "decode": ["k_decode_bf16.cu", "k_paging.cu", "internal.h", "tc_ptx.cuh"],
+    "decode": ["k_decode_shared.cu", "decode_plan.cu", "k_paging.cu", "internal.h", "tc_ptx.cuh"],
     "prefill": ["k_prefill_tc.cu", "internal.h", "tc_ptx.cuh"],
 }
 # RoPE variants the bench can time: the kernels' work does not depend on the
@@ -69,10 +70,10 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    ("llama3_8b", "decode"): (69.25e6, "b19624a9cee07e87"),
-    ("llama3_8b", "prefill"): (77.89e6, "0c435da0e4b12845"),
-    ("few_shot_skewed", "decode"): (494.20e6, "b19624a9cee07e87"),
-    ("few_shot_skewed", "prefill"): (599.04e6, "0c435da0e4b12845"),
+    # decode call = decode_shared 4,636,032,768 + 72,134,144; combine 70,302,208 + 229,120;
+    # append 299,520 (read + write bytes); prefill 8,542,410,752 + 260,228,096
+    ("llama3_70b", "decode"): (4778997760.0, "b1006cea44273475"),
+    ("llama3_70b", "prefill"): (8802638848.0, "492e39bcf0b528b3"),
 }
 
 
