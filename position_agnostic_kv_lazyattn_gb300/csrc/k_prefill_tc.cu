@@ -11,8 +11,10 @@
 // (query token, query head of the group) pair, so every K/V tile and its
 // rotation serve 256 rows of the group. Tiles of 128 keys (8 pages) stream
 // through two-stage K and V rings. Roles (16 warps = 4 warpgroups):
-//   warps 0, 2    TMA producers, K ring and V ring: per tile 8 pages x two
-//                 64-dim boxes (128B swizzle); with K, each page's row
+//   warps 0, 2    TMA producers, K ring and V ring: per tile two groups of
+//                 four pages, each group one box of four consecutive pages
+//                 per 64-dim half when its pages are consecutive (else a box
+//                 per page; 128B swizzle); with K, each page's row
 //                 (cos, sin)(start * theta) of the position table (bulk copy)
 //                 and the tile's page starts / token counts in a 4-deep ring
 //   warp 1        TMEM owner and single-thread UMMA issuer, per tile k:
@@ -78,6 +80,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // What the producer tells the consumers about a tile.
 struct TileInfo {
     int j;                        // tile index, -1: no more tiles
+    int consec;                   // bit b: pages 4b .. 4b+3 are consecutive pages, all with keys
+    int page[2];                  // first page of each group of four
     int start[kPagesPerTile];     // logical position of slot 0 of each page
     int n[kPagesPerTile];         // keys in each page (0: none / unusable)
     int y[kPagesPerTile];         // row of the page in the K/V tensor maps (out of range: zero fill)
@@ -144,7 +148,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
     return o;
 }
-
 // Entry check shared by every role so that all of them agree on which slots
 // hold keys: page in range and positions inside the table.
 __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
@@ -162,7 +165,8 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 // (§3.5, score-space positional methods), computed from logical positions.
 template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, PoolView pv,
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4, PoolView pv,
                       PrefillParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,21 +287,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ds = smem_u32(sm + kOffK + st * kKVBytes);
                     const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
                     int ys[kPagesPerTile];
+                    int consec = 3;
 #pragma unroll
                     for (int p = 0; p < kPagesPerTile; ++p) {
                         if (n[p] < 0) record_error(pv.status, LAZYATTN_ERANGE);
                         ys[p] = n[p] > 0 ? ((int)entry_page(cur[p]) * Hkv + h) * kPage : P.oob_row;
+                        if (n[p] <= 0 || entry_page(cur[p]) != entry_page(cur[p & ~3]) + (uint32_t)(p & 3))
+                            consec &= ~(1 << (p >> 2));
                         info.start[p] = entry_start(cur[p]);
                         info.n[p] = max(n[p], 0);
                         info.y[p] = ys[p];
                     }
                     info.j = j;
+                    info.consec = consec;
+                    info.page[0] = (int)entry_page(cur[0]);
+                    info.page[1] = (int)entry_page(cur[4]);
                     mbar_arrive(ib);   // releases the info writes to the other roles
                     mbar_arrive_expect_tx(fb, kKVBytes + kBaseBytes);
 #pragma unroll
+                    for (int b4 = 0; b4 < 2; ++b4) {
+                        if (consec & (1 << b4)) {   // four consecutive pages: one box per half of the dims
+                            const int pg = (int)entry_page(cur[4 * b4]);
+                            tma_load_4d(ds + b4 * 8192, &kmap4, 0, 0, h, pg, fb);
+                            tma_load_4d(ds + kKVChunk + b4 * 8192, &kmap4, 64, 0, h, pg, fb);
+                        } else {
+#pragma unroll
+                            for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
+                                tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
+                                tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
+                            }
+                        }
+                    }
+#pragma unroll
                     for (int p = 0; p < kPagesPerTile; ++p) {
-                        tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
-                        tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
                         const int rowpos = LOCAL ? curd[p] : entry_start(cur[p]);   // position of the page's rotation
                         const float2* base = pv.rope + (n[p] > 0 ? (size_t)rowpos * (kD / 2) : 0);
                         bulk_load(bs + p * 512, base, 512, fb);
@@ -336,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int ys[kPagesPerTile];
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) ys[p] = info.y[p];
+                const int consec = info.consec, pg0 = info.page[0], pg1 = info.page[1];
                 if (k >= kStages && !mbar_wait(smem_u32(&bar_vempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -344,9 +367,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ds = smem_u32(sm + kOffV + st * kKVBytes);
                 mbar_arrive_expect_tx(fb, kKVBytes);
 #pragma unroll
-                for (int p = 0; p < kPagesPerTile; ++p) {
-                    tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
-                    tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                for (int b4 = 0; b4 < 2; ++b4) {
+                    if (consec & (1 << b4)) {
+                        const int pg = b4 ? pg1 : pg0;
+                        tma_load_4d(ds + b4 * 8192, &vmap4, 0, 0, h, pg, fb);
+                        tma_load_4d(ds + kKVChunk + b4 * 8192, &vmap4, 64, 0, h, pg, fb);
+                    } else {
+#pragma unroll
+                        for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
+                            tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
+                            tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                        }
+                    }
                 }
                 last_k[st] = k;
             }
@@ -439,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rt = threadIdx.x - 384;
         const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
         float cs[8], sn[8];   // (cos, sin)(slot * theta_f), f = 8u + 0..7
-        {
+        if (!PREROT && !ALIBI && !LOCAL) {
             const float4* t4 = reinterpret_cast<const float4*>(pv.rope + (size_t)slot * (kD / 2) + 8 * u);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -482,15 +514,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < kPagesPerTile; ++p) n[p] = info.n[p];
             uint8_t* kb = sm + kOffK + st * kKVBytes;
             const uint8_t* bb = sm + kOffBase + st * kBaseBytes + u * 64;
-#pragma unroll 2
-            for (int p = 0; p < kPagesPerTile; ++p) {
-                const int kr = p * kPage + slot;
-                uint4* p1 = reinterpret_cast<uint4*>(kb + sw128_offset(kr, u));
-                uint4* p2 = reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u));
-                if (slot < n[p]) {
+            // Two pages at a time: both pages' loads before the first store,
+            // so that their latencies overlap (the loop body stays compact:
+            // the four roles' code shares the instruction caches).
+#pragma unroll 1
+            for (int h4 = 0; h4 < 8 / 2; ++h4) {
+                uint4 w1[2], w2[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int kr = (2 * h4 + q) * kPage + slot;
+                    w1[q] = *reinterpret_cast<const uint4*>(kb + sw128_offset(kr, u));
+                    w2[q] = *reinterpret_cast<const uint4*>(kb + kKVChunk + sw128_offset(kr, u));
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int p = 2 * h4 + q;
                     float x1[8], x2[8];
-                    unpack8(*p1, x1);
-                    unpack8(*p2, x2);
+                    unpack8(w1[q], x1);
+                    unpack8(w2[q], x2);
                     if (!PREROT && !ALIBI) {
                         const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
@@ -502,18 +543,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float cb = w ? b.z : b.x, sb = w ? b.w : b.y;
                                 // LOCAL: the page's one relative rotation; else start + slot
                                 const float c = LOCAL ? cb : cb * cs[f] - sb * sn[f];
-                                const float s = LOCAL ? sb : sb * cs[f] + cb * sn[f];
+                                const float s_ = LOCAL ? sb : sb * cs[f] + cb * sn[f];
                                 const float a = x1[f], z = x2[f];
-                                x1[f] = a * c - z * s;
-                                x2[f] = a * s + z * c;
+                                x1[f] = a * c - z * s_;
+                                x2[f] = a * s_ + z * c;
                             }
                         }
                     }
-                    *p1 = pack8_h(x1);
-                    *p2 = pack8_h(x2);
-                } else {   // no key in this slot: zero K so that its scores stay finite
-                    *p1 = make_uint4(0, 0, 0, 0);
-                    *p2 = make_uint4(0, 0, 0, 0);
+                    // no key in this slot: zero K so that its scores stay finite
+                    const bool key = slot < n[p];
+                    w1[q] = key ? pack8_h(x1) : make_uint4(0, 0, 0, 0);
+                    w2[q] = key ? pack8_h(x2) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int kr = (2 * h4 + q) * kPage + slot;
+                    *reinterpret_cast<uint4*>(kb + sw128_offset(kr, u)) = w1[q];
+                    *reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u)) = w2[q];
                 }
             }
             // V needs no work here: pages without keys are not read (their rows
@@ -770,7 +816,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, PoolView, PrefillParams);
+using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, PoolView,
+                               PrefillParams);
 
 // The instantiation for a pool and a batch: key layout and pairing of the pool,
 // pre-rotated pages of the batch.
@@ -815,7 +862,7 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     auto kern = prefill_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0,
                                    p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0,
                                    p.d.position_encoding == LAZYATTN_POS_ALIBI);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.view(), P);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.kmap4, p.vmap4, p.view(), P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }
 
