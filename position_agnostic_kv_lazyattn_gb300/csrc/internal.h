@@ -188,6 +188,10 @@ struct lazyattn_pool {
     bool have_maps = false;            // bf16 pools: TMA views of the K and V pools
     CUtensorMap kmap, vmap;            // rows of 128 dims, boxes of one page (64 dims x 16 slots)
     CUtensorMap kmap4, vmap4;          // {D, slot, KV head, page}, boxes of four consecutive pages
+    CUtensorMap kmap8, vmap8;          // the same view, boxes of eight consecutive pages
+    bool have_rmap = false;            // rmap encoded (position tables of at least 128 rows)
+    CUtensorMap rmap;                  // position table as {2 * (D/2) floats, 16, max_position / 16}:
+                                       // a box holds rows p, p + 16, ..., p + 112 (eight pages' starts)
     lazyattn::PoolView view() const;
 };
 

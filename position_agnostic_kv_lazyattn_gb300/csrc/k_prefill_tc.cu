@@ -11,12 +11,16 @@
 // (query token, query head of the group) pair, so every K/V tile and its
 // rotation serve 256 rows of the group. Tiles of 128 keys (8 pages) stream
 // through two-stage K and V rings. Roles (16 warps = 4 warpgroups):
-//   warps 0, 2    TMA producers, K ring and V ring: per tile two groups of
-//                 four pages, each group one box of four consecutive pages
-//                 per 64-dim half when its pages are consecutive (else a box
-//                 per page; 128B swizzle); with K, each page's row
-//                 (cos, sin)(start * theta) of the position table (bulk copy)
-//                 and the tile's page starts / token counts in a 4-deep ring
+//   warps 0, 2    TMA producers, K ring and V ring: per 64-dim half one box
+//                 of eight consecutive pages, else of four, else one per page
+//                 (128B swizzle); with K, each page's row (cos, sin)(start *
+//                 theta) of the position table (one strided box when the pages
+//                 start 16 positions apart, else a bulk copy per page) and the
+//                 tile's page starts / token counts in a 4-deep ring. Copy
+//                 instructions cost the issuing thread tens of nanoseconds each,
+//                 so the K producer computes a tile's boxes and info while it
+//                 waits for the stage, issues the copies first and writes the
+//                 info after them
 //   warp 1        TMEM owner and single-thread UMMA issuer, per tile k:
 //                 S_0 = Q_0 K^T; O_1 += P_1 V (tile k-1); S_1 = Q_1 K^T;
 //                 O_0 += P_0 V (tile k). QK is fp16 128x128x128 from shared
@@ -77,10 +81,13 @@ constexpr float kRescaleThreshold = 8.0f;          // log2 units
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzled tiles need 1 KB alignment");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// What the producer tells the consumers about a tile.
-struct TileInfo {
+// What the producer tells the consumers about a tile (written with 16-byte
+// stores: the producer's stores queue behind the math roles' shared-memory
+// traffic).
+struct __align__(16) TileInfo {
     int j;                        // tile index, -1: no more tiles
-    int consec;                   // bit b: pages 4b .. 4b+3 are consecutive pages, all with keys
+    int consec;                   // bit b < 2: pages 4b .. 4b+3 are consecutive pages, all with keys;
+                                  // bit 2: all eight are
     int page[2];                  // first page of each group of four
     int start[kPagesPerTile];     // logical position of slot 0 of each page
     int n[kPagesPerTile];         // keys in each page (0: none / unusable)
@@ -98,6 +105,7 @@ struct PrefillParams {
     int32_t g;
     int32_t oob_row;     // a row index outside the K/V tensor maps: TMA fills zeros
     const int32_t* entry_delta;   // doc-local pools: document offset of each entry
+    int32_t row_blocks;           // rows of the position-table view (max_position / 16); 0: no view
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -166,8 +174,11 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4, PoolView pv,
-                      PrefillParams P) {
+                      const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4,
+                      const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
+                      const __grid_constant__ CUtensorMap rmap, PoolView pv, PrefillParams P) {
+    constexpr bool ROT = !PREROT && !ALIBI;   // K rotated here: the pages' position-table rows are loaded
+    static_assert(sizeof(TileInfo) == 7 * 16, "tile info layout (written as seven 16-byte words)");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -271,6 +282,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (j == T || live) {
                     const int st = k % kStages;
+                    // Everything the tile's copies and info need, before the wait.
+                    int ys[kPagesPerTile], nn[kPagesPerTile], ss[kPagesPerTile];
+                    int consec = 3;
+                    bool bad = false;
+#pragma unroll
+                    for (int p = 0; p < kPagesPerTile; ++p) {
+                        bad = bad || n[p] < 0;
+                        nn[p] = max(n[p], 0);
+                        ss[p] = entry_start(cur[p]);
+                        ys[p] = n[p] > 0 ? ((int)entry_page(cur[p]) * Hkv + h) * kPage : P.oob_row;
+                        if (n[p] <= 0 || entry_page(cur[p]) != entry_page(cur[p & ~3]) + (uint32_t)(p & 3))
+                            consec &= ~(1 << (p >> 2));
+                    }
+                    const int pg0 = (int)entry_page(cur[0]), pg1 = (int)entry_page(cur[4]);
+                    if (consec == 3 && pg1 == pg0 + 4) consec |= 4;
+                    // The pages' rows: when the eight pages start 16 positions apart
+                    // (full pages at consecutive positions), one box of the position
+                    // table's 16-row view; else a copy per page.
+                    const int t0 = ss[0];
+                    bool strided = ROT && !LOCAL && P.row_blocks > 0 && t0 / kPage + kPagesPerTile <= P.row_blocks;
+#pragma unroll
+                    for (int p = 0; p < kPagesPerTile; ++p) strided = strided && n[p] > 0 && ss[p] == t0 + kPage * p;
                     if (k >= kStages && !mbar_wait(smem_u32(&bar_kempty[st]), ((k / kStages) - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -286,44 +319,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t ds = smem_u32(sm + kOffK + st * kKVBytes);
                     const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
-                    int ys[kPagesPerTile];
-                    int consec = 3;
+                    // Copies first (each copy instruction costs this thread tens of
+                    // nanoseconds, so eight consecutive pages take one box per half
+                    // of the dims); the stage's own arrival comes after the info
+                    // writes, so a consumer that sees the stage full sees the info.
+                    mbar_expect_tx(fb, kKVBytes + (ROT ? kBaseBytes : 0));
+                    if (consec & 4) {
+                        tma_load_4d(ds, &kmap8, 0, 0, h, pg0, fb);
+                        tma_load_4d(ds + kKVChunk, &kmap8, 64, 0, h, pg0, fb);
+                    } else {
 #pragma unroll
-                    for (int p = 0; p < kPagesPerTile; ++p) {
-                        if (n[p] < 0) record_error(pv.status, LAZYATTN_ERANGE);
-                        ys[p] = n[p] > 0 ? ((int)entry_page(cur[p]) * Hkv + h) * kPage : P.oob_row;
-                        if (n[p] <= 0 || entry_page(cur[p]) != entry_page(cur[p & ~3]) + (uint32_t)(p & 3))
-                            consec &= ~(1 << (p >> 2));
-                        info.start[p] = entry_start(cur[p]);
-                        info.n[p] = max(n[p], 0);
-                        info.y[p] = ys[p];
-                    }
-                    info.j = j;
-                    info.consec = consec;
-                    info.page[0] = (int)entry_page(cur[0]);
-                    info.page[1] = (int)entry_page(cur[4]);
-                    mbar_arrive(ib);   // releases the info writes to the other roles
-                    mbar_arrive_expect_tx(fb, kKVBytes + kBaseBytes);
+                        for (int b4 = 0; b4 < 2; ++b4) {
+                            if (consec & (1 << b4)) {   // four consecutive pages: one box per half of the dims
+                                const int pg = b4 ? pg1 : pg0;
+                                tma_load_4d(ds + b4 * 8192, &kmap4, 0, 0, h, pg, fb);
+                                tma_load_4d(ds + kKVChunk + b4 * 8192, &kmap4, 64, 0, h, pg, fb);
+                            } else {
 #pragma unroll
-                    for (int b4 = 0; b4 < 2; ++b4) {
-                        if (consec & (1 << b4)) {   // four consecutive pages: one box per half of the dims
-                            const int pg = (int)entry_page(cur[4 * b4]);
-                            tma_load_4d(ds + b4 * 8192, &kmap4, 0, 0, h, pg, fb);
-                            tma_load_4d(ds + kKVChunk + b4 * 8192, &kmap4, 64, 0, h, pg, fb);
-                        } else {
-#pragma unroll
-                            for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
-                                tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
-                                tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
+                                for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
+                                    tma_load_2d(ds + p * 2048, &kmap, 0, ys[p], fb);
+                                    tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
+                                }
                             }
                         }
                     }
+                    if (strided) {
+                        tma_load_3d(bs, &rmap, 0, t0 % kPage, t0 / kPage, fb);
+                    } else if (ROT) {
 #pragma unroll
-                    for (int p = 0; p < kPagesPerTile; ++p) {
-                        const int rowpos = LOCAL ? curd[p] : entry_start(cur[p]);   // position of the page's rotation
-                        const float2* base = pv.rope + (n[p] > 0 ? (size_t)rowpos * (kD / 2) : 0);
-                        bulk_load(bs + p * 512, base, 512, fb);
+                        for (int p = 0; p < kPagesPerTile; ++p) {
+                            const int rowpos = LOCAL ? curd[p] : ss[p];   // position of the page's rotation
+                            const float2* base = pv.rope + (n[p] > 0 ? (size_t)rowpos * (kD / 2) : 0);
+                            bulk_load(bs + p * 512, base, 512, fb);
+                        }
                     }
+                    int4* iv = reinterpret_cast<int4*>(&info);
+                    iv[0] = make_int4(j, consec, pg0, pg1);
+                    iv[1] = make_int4(ss[0], ss[1], ss[2], ss[3]);
+                    iv[2] = make_int4(ss[4], ss[5], ss[6], ss[7]);
+                    iv[3] = make_int4(nn[0], nn[1], nn[2], nn[3]);
+                    iv[4] = make_int4(nn[4], nn[5], nn[6], nn[7]);
+                    iv[5] = make_int4(ys[0], ys[1], ys[2], ys[3]);
+                    iv[6] = make_int4(ys[4], ys[5], ys[6], ys[7]);
+                    mbar_arrive(ib);   // releases the info writes to the other roles
+                    mbar_arrive(fb);
+                    if (bad) record_error(pv.status, LAZYATTN_ERANGE);
                     last_k[st] = k;
                     ++k;
                 }
@@ -366,17 +406,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = smem_u32(&bar_vfull[st]);
                 const uint32_t ds = smem_u32(sm + kOffV + st * kKVBytes);
                 mbar_arrive_expect_tx(fb, kKVBytes);
+                if (consec & 4) {
+                    tma_load_4d(ds, &vmap8, 0, 0, h, pg0, fb);
+                    tma_load_4d(ds + kKVChunk, &vmap8, 64, 0, h, pg0, fb);
+                } else {
 #pragma unroll
-                for (int b4 = 0; b4 < 2; ++b4) {
-                    if (consec & (1 << b4)) {
-                        const int pg = b4 ? pg1 : pg0;
-                        tma_load_4d(ds + b4 * 8192, &vmap4, 0, 0, h, pg, fb);
-                        tma_load_4d(ds + kKVChunk + b4 * 8192, &vmap4, 64, 0, h, pg, fb);
-                    } else {
+                    for (int b4 = 0; b4 < 2; ++b4) {
+                        if (consec & (1 << b4)) {
+                            const int pg = b4 ? pg1 : pg0;
+                            tma_load_4d(ds + b4 * 8192, &vmap4, 0, 0, h, pg, fb);
+                            tma_load_4d(ds + kKVChunk + b4 * 8192, &vmap4, 64, 0, h, pg, fb);
+                        } else {
 #pragma unroll
-                        for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
-                            tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
-                            tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                            for (int p = 4 * b4; p < 4 * b4 + 4; ++p) {
+                                tma_load_2d(ds + p * 2048, &vmap, 0, ys[p], fb);
+                                tma_load_2d(ds + kKVChunk + p * 2048, &vmap, 64, ys[p], fb);
+                            }
                         }
                     }
                 }
@@ -816,8 +861,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, PoolView,
-                               PrefillParams);
+using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                               const CUtensorMap, const CUtensorMap, const CUtensorMap, PoolView, PrefillParams);
 
 // The instantiation for a pool and a batch: key layout and pairing of the pool,
 // pre-rotated pages of the batch.
@@ -857,12 +902,14 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     P.g = g;
     P.oob_row = (int32_t)rows;
     P.entry_delta = b.entry_delta;
+    P.row_blocks = p.have_rmap ? p.d.max_position / kPage : 0;
     const int TQ = kRows / g;
     dim3 grid((b.max_q_len + TQ - 1) / TQ, p.d.n_kv_heads, b.num_requests);
     auto kern = prefill_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0,
                                    p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0,
                                    p.d.position_encoding == LAZYATTN_POS_ALIBI);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.kmap4, p.vmap4, p.view(), P);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.kmap4, p.vmap4, p.kmap8, p.vmap8, p.rmap, p.view(),
+                                                 P);
     return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
 }
 

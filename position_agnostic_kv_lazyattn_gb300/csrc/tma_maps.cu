@@ -32,16 +32,33 @@ bool encode_one(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* b
 }
 
 // The same pool as a 4-D tensor {D, slot, KV head, page} (strides 2 B, D * 2 B,
-// 16 * D * 2 B, Hkv * 16 * D * 2 B) with boxes {64, 16, 1, 4}: one box holds
-// half the dims of four consecutive pages of one KV head, rows ordered
-// (page, slot) exactly as four 2-D page boxes side by side.
-bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t pages, int hkv, int d) {
+// 16 * D * 2 B, Hkv * 16 * D * 2 B) with boxes {64, 16, 1, run}: one box holds
+// half the dims of `run` consecutive pages of one KV head, rows ordered
+// (page, slot) exactly as `run` 2-D page boxes side by side.
+bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t pages, int hkv, int d,
+                uint32_t run) {
     cuuint64_t gdim[4] = {(cuuint64_t)d, (cuuint64_t)kPage, (cuuint64_t)hkv, (cuuint64_t)pages};
     cuuint64_t gstride[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * kPage, (cuuint64_t)d * 2 * kPage * hkv};
-    cuuint32_t box[4] = {64, (cuuint32_t)kPage, 1, 4};
+    cuuint32_t box[4] = {64, (cuuint32_t)kPage, 1, run};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, gdim, gstride, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The position table (float2 (cos, sin) rows of D/2 frequencies, one row per
+// position) as a 3-D fp32 tensor {D, 16, max_position / 16} (strides 4 B,
+// 2 D B, 32 D B): a box {D, 1, 8} at (0, t % 16, t / 16) holds the rows of
+// positions t, t + 16, ..., t + 112, i.e. the start rows of eight pages that
+// follow each other at consecutive positions. Positions past the last whole
+// block of 16 are outside the view (callers copy those rows one by one).
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, int32_t max_position, int d) {
+    cuuint64_t gdim[3] = {(cuuint64_t)d, (cuuint64_t)kPage, (cuuint64_t)(max_position / kPage)};
+    cuuint64_t gstride[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * kPage};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, 8};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -49,6 +66,7 @@ bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* b
 
 bool encode_pool_maps(lazyattn_pool& p) {
     p.have_maps = false;
+    p.have_rmap = false;
     if (p.d.dtype != LAZYATTN_BF16) return false;
     const uint64_t rows = (uint64_t)p.d.num_pages * (uint64_t)p.d.n_kv_heads * kPage;
     if (rows + kPage > (uint64_t)INT_MAX) return false;
@@ -56,8 +74,12 @@ bool encode_pool_maps(lazyattn_pool& p) {
     if (!enc) return false;
     if (!encode_one(enc, &p.kmap, p.d.k_pool, rows, p.d.head_dim)) return false;
     if (!encode_one(enc, &p.vmap, p.d.v_pool, rows, p.d.head_dim)) return false;
-    if (!encode_run(enc, &p.kmap4, p.d.k_pool, (uint64_t)p.d.num_pages, p.d.n_kv_heads, p.d.head_dim)) return false;
-    if (!encode_run(enc, &p.vmap4, p.d.v_pool, (uint64_t)p.d.num_pages, p.d.n_kv_heads, p.d.head_dim)) return false;
+    const uint64_t np = (uint64_t)p.d.num_pages;
+    const int hkv = p.d.n_kv_heads, d = p.d.head_dim;
+    if (!encode_run(enc, &p.kmap4, p.d.k_pool, np, hkv, d, 4) || !encode_run(enc, &p.vmap4, p.d.v_pool, np, hkv, d, 4) ||
+        !encode_run(enc, &p.kmap8, p.d.k_pool, np, hkv, d, 8) || !encode_run(enc, &p.vmap8, p.d.v_pool, np, hkv, d, 8))
+        return false;
+    p.have_rmap = p.d.max_position >= 8 * kPage && encode_rows(enc, &p.rmap, p.d.rope_table, p.d.max_position, d);
     p.have_maps = true;
     return true;
 }
