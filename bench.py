@@ -241,6 +241,15 @@ def run_ours(args, rank, world):
         """A workspace for decode calls on batch (its own plan may need more)."""
         n = L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_DECODE, batch.c)
         return (ws, ws_bytes) if n <= ws_bytes else (torch.zeros((n + 3) // 4, dtype=torch.int32, device=dev), n)
+
+    pws = {}
+
+    def pws_for(batch):
+        """The prefill workspace of batch (room for the partials of a split prefill)."""
+        n = L.lazyattn_workspace_size(env.pool.handle, L.LAZYATTN_OP_PREFILL, batch.c)
+        if n not in pws:
+            pws[n] = torch.zeros((n + 3) // 4, dtype=torch.int32, device=dev)
+        return pws[n], n
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # > 129 MB L2
 
     def ev():
@@ -259,7 +268,8 @@ def run_ours(args, rank, world):
         return g
 
     def prefill_fn(batch):
-        return lambda: L.lazyattn_prefill(env.pool.handle, batch.c, env.q, out_p, None, 0, None)
+        w, wb = pws_for(batch)
+        return lambda: L.lazyattn_prefill(env.pool.handle, batch.c, env.q, out_p, w, wb, None)
 
     def decode_fn(batch, t):
         q, k, v = dec_in[t]
@@ -393,13 +403,14 @@ def run_ours(args, rank, world):
             q_host = env.q.cpu().pin_memory()
             o_host = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
             q_dev = torch.empty_like(env.q)
+            pw, pwb = pws_for(b)
             per_rep = []
             for _ in range(reps):
                 flush.zero_()
                 a, z = ev(), ev()
                 a.record(stream)
                 q_dev.copy_(q_host, non_blocking=True)
-                L.lazyattn_prefill(env.pool.handle, b.c, q_dev, out_p, None, 0, stream)
+                L.lazyattn_prefill(env.pool.handle, b.c, q_dev, out_p, pw, pwb, stream)
                 o_host.copy_(out_p, non_blocking=True)
                 z.record(stream)
                 torch.cuda.synchronize()

@@ -298,7 +298,14 @@ size_t lazyattn_workspace_size(lazyattn_pool_t pool, int32_t op, const lazyattn_
  * (unless LAZYATTN_KEYS_PREROTATED), scale 1/sqrt(head_dim). The query
  * segment's own K/V must already be stored and listed in the entries. Entries
  * with nvalid = 0 contribute nothing. A row that sees no key gets zeros.
- * Pool pages are only read. */
+ * Pool pages are only read.
+ * workspace (optional, device, 256-byte aligned, no zero-fill needed): with at
+ * least lazyattn_workspace_size(pool, LAZYATTN_OP_PREFILL, batch) bytes, bf16
+ * pools may split each (request, KV head, query pair)'s KV tiles over 2..4 CTAs
+ * when the batch fills few waves of the GPU, and merge their partial outputs
+ * (per row: reference maximum, sum, unnormalised O) in a second kernel on the
+ * same stream; NULL or fewer bytes: one CTA per item. Both give results within
+ * the same error bounds. */
 int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q, void* out,
                      void* workspace, size_t workspace_bytes, void* stream);
 

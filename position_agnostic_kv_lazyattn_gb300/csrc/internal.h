@@ -236,7 +236,11 @@ int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const 
 // sets the kernel's shared-memory limit on the current device (done once, at
 // pool creation, so that launches stay capturable in CUDA graphs).
 int prefill_init();
+// Split count of a bf16 prefill over the KV tiles (1: one CTA per request, KV
+// head and query pair) and the workspace bytes its partials take.
+int prefill_splits(const lazyattn_pool& p, const lazyattn_batch& b);
+size_t prefill_ws_bytes(const lazyattn_pool& p, const lazyattn_batch& b, int splits);
 int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
-                        __nv_bfloat16* out, cudaStream_t stream);
+                        __nv_bfloat16* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace lazyattn

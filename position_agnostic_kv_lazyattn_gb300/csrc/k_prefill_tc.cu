@@ -106,6 +106,10 @@ struct PrefillParams {
     int32_t oob_row;     // a row index outside the K/V tensor maps: TMA fills zeros
     const int32_t* entry_delta;   // doc-local pools: document offset of each entry
     int32_t row_blocks;           // rows of the position-table view (max_position / 16); 0: no view
+    int32_t splits;               // CTAs per (request, KV head, query pair), each a share of the tiles
+    int32_t qpairs;               // query pairs per request (grid.x / splits)
+    float* part_o;                // splits > 1: [item][split][row][D] unnormalised O
+    float2* part_ml;              // splits > 1: [item][split][row] (reference maximum, sum)
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -171,7 +175,9 @@ __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
 // INTER: q arrives with interleaved RoPE pairs and is de-interleaved on load.
 // ALIBI: no rotation of q or k; each score gets the bias -slope_h (m - n)
 // (§3.5, score-space positional methods), computed from logical positions.
-template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
+// SPLIT: the request's tiles are shared by P.splits CTAs, each writing partials
+// (a separate instantiation, so that the unsplit kernel's code is unchanged).
+template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4,
@@ -190,7 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    const int qp = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
+    const int qp = SPLIT ? (int)blockIdx.x / P.splits : (int)blockIdx.x;
+    const int split = SPLIT ? (int)blockIdx.x - qp * P.splits : 0;
+    const int h = blockIdx.y, r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = P.g, Hq = pv.hq, Hkv = pv.hkv;
     const int TQ = kRows / g;                  // query tokens per CTA
@@ -207,7 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qs = P.q_start[r];
     const int m_hi = qs + i0 + ntok - 1;       // largest query position of the CTA
     const int e0 = P.entry_offsets[r], e1 = P.entry_offsets[r + 1];
-    const int T = e1 > e0 ? (e1 - e0 + kPagesPerTile - 1) / kPagesPerTile : 0;
+    // This CTA's share of the request's tiles: [jb, jb + T)
+    const int t_all = e1 > e0 ? (e1 - e0 + kPagesPerTile - 1) / kPagesPerTile : 0;
+    const int chunk = SPLIT ? (t_all + P.splits - 1) / P.splits : t_all;
+    const int jb = SPLIT ? min(t_all, split * chunk) : 0;
+    const int T = SPLIT ? min(t_all, jb + chunk) - jb : t_all;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -254,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_entries = [&](int jj, uint64_t (&e)[kPagesPerTile], int (&dl)[kPagesPerTile]) {
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
-                    const int idx = e0 + jj * kPagesPerTile + p;
+                    const int idx = e0 + (jb + jj) * kPagesPerTile + p;
                     const uint64_t v = P.entries[min(idx, e1 - 1)];
                     e[p] = idx < e1 ? v : 0ull;   // 0: an empty entry
                     if (LOCAL) dl[p] = P.entry_delta[min(idx, e1 - 1)];
@@ -822,8 +834,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bar_pfull[qi]));
         }
 
-        // epilogue: O / l -> bf16 rows of out
-        if (active) {
+        // epilogue: O / l -> bf16 rows of out; or, when the request's tiles are
+        // split over several CTAs, this CTA's unnormalised O with its reference
+        // maximum and sum (merged by prefill_combine_kernel)
+        if (SPLIT && active) {
+            if (ok && k >= 1) ok = mbar_wait(smem_u32(&bar_odone[qi]), (k - 1) & 1, abort_flag);
+            tc_fence_after();
+            const size_t slot = ((size_t)((r * Hkv + h) * P.qpairs + qp) * P.splits + split) * kRows + row;
+            const bool keys = ok && k >= 1 && l_run > 0.f;
+            if (t_local < ntok) P.part_ml[slot] = make_float2(m_run == -INFINITY ? 0.f : m_run, keys ? l_run : 0.f);
+            if (k >= 1 && ok) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(to + 32 * c, v);
+                    if (keys && t_local < ntok) {
+                        float4* dst = reinterpret_cast<float4*>(P.part_o + slot * kD + 32 * c);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    }
+                }
+            }
+        } else if (active) {
             if (ok && k >= 1) ok = mbar_wait(smem_u32(&bar_odone[qi]), (k - 1) & 1, abort_flag);
             tc_fence_after();
             __nv_bfloat16* op = P.out + ((size_t)(q0 + tok) * Hq + (size_t)h * g + jh) * kD;
@@ -859,6 +893,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Merge of a split prefill: thread = (row of an item, 8 dims); the partials
+// with a positive sum are weighted by 2^(m_s - M), M their largest reference
+// maximum (the kernel's scores are in the log2 domain).
+__global__ void __launch_bounds__(256)
+    prefill_combine_kernel(PoolView pv, PrefillParams P) {
+    const int item = blockIdx.x, row = blockIdx.y * 16 + (threadIdx.x >> 4), d0 = (threadIdx.x & 15) * 8;
+    const int g = P.g, Hkv = pv.hkv;
+    const int qp = item % P.qpairs, h = (item / P.qpairs) % Hkv, r = item / (P.qpairs * Hkv);
+    const int TQ = kRows / g;
+    const int q0 = P.q_offsets[r], q1 = P.q_offsets[r + 1];
+    const int tok = qp * TQ + row / g, jh = row % g;
+    if (tok >= q1 - q0) return;
+    const size_t base = (size_t)item * P.splits * kRows + row;
+    float M = -INFINITY;
+    for (int sp = 0; sp < P.splits; ++sp) {
+        const float2 x = __ldcg(&P.part_ml[base + (size_t)sp * kRows]);
+        if (x.y > 0.f) M = fmaxf(M, x.x);
+    }
+    float L = 0.f, a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.f;
+    if (M != -INFINITY) {
+        for (int sp = 0; sp < P.splits; ++sp) {
+            const size_t slot = base + (size_t)sp * kRows;
+            const float2 x = __ldcg(&P.part_ml[slot]);
+            if (!(x.y > 0.f)) continue;
+            const float w = fast_exp2(x.x - M);
+            L += x.y * w;
+            const float4* src = reinterpret_cast<const float4*>(P.part_o + slot * kD + d0);
+            const float4 s0 = __ldcg(src), s1 = __ldcg(src + 1);
+            a[0] += s0.x * w; a[1] += s0.y * w; a[2] += s0.z * w; a[3] += s0.w * w;
+            a[4] += s1.x * w; a[5] += s1.y * w; a[6] += s1.z * w; a[7] += s1.w * w;
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + tok) * pv.hq + (size_t)h * g + jh) * kD + d0);
+    *dst = make_uint4(pack_bf2(a[0] * inv, a[1] * inv), pack_bf2(a[2] * inv, a[3] * inv),
+                      pack_bf2(a[4] * inv, a[5] * inv), pack_bf2(a[6] * inv, a[7] * inv));
+}
+
 }  // namespace
 
 using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
@@ -866,26 +940,76 @@ using PrefillKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUten
 
 // The instantiation for a pool and a batch: key layout and pairing of the pool,
 // pre-rotated pages of the batch.
-PrefillKernel prefill_kernel_for(bool prerot, bool local, bool inter, bool alibi) {
-    if (alibi) return prefill_tc_kernel<false, false, false, true>;
-    if (local) return inter ? prefill_tc_kernel<false, true, true, false> : prefill_tc_kernel<false, true, false, false>;
-    if (prerot) return inter ? prefill_tc_kernel<true, false, true, false> : prefill_tc_kernel<true, false, false, false>;
-    return inter ? prefill_tc_kernel<false, false, true, false> : prefill_tc_kernel<false, false, false, false>;
+template <bool SPLIT>
+PrefillKernel prefill_kernel_variant(bool prerot, bool local, bool inter, bool alibi) {
+    if (alibi) return prefill_tc_kernel<false, false, false, true, SPLIT>;
+    if (local)
+        return inter ? prefill_tc_kernel<false, true, true, false, SPLIT> : prefill_tc_kernel<false, true, false, false, SPLIT>;
+    if (prerot)
+        return inter ? prefill_tc_kernel<true, false, true, false, SPLIT> : prefill_tc_kernel<true, false, false, false, SPLIT>;
+    return inter ? prefill_tc_kernel<false, false, true, false, SPLIT> : prefill_tc_kernel<false, false, false, false, SPLIT>;
+}
+
+PrefillKernel prefill_kernel_for(bool prerot, bool local, bool inter, bool alibi, bool split) {
+    return split ? prefill_kernel_variant<true>(prerot, local, inter, alibi)
+                 : prefill_kernel_variant<false>(prerot, local, inter, alibi);
 }
 
 int prefill_init() {
-    for (int i = 0; i < 9; ++i) {
-        if (i < 8 && (i & 1) && (i & 2)) continue;   // pre-rotated pages are never doc-local
-        PrefillKernel k = i == 8 ? prefill_kernel_for(false, false, false, true)
-                                 : prefill_kernel_for(i & 1, i & 2, i & 4, false);
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-            return LAZYATTN_ECUDA;
-    }
+    for (int sp = 0; sp < 2; ++sp)
+        for (int i = 0; i < 9; ++i) {
+            if (i < 8 && (i & 1) && (i & 2)) continue;   // pre-rotated pages are never doc-local
+            PrefillKernel k = i == 8 ? prefill_kernel_for(false, false, false, true, sp)
+                                     : prefill_kernel_for(i & 1, i & 2, i & 4, false, sp);
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+                return LAZYATTN_ECUDA;
+        }
     return LAZYATTN_OK;
 }
 
+// Split count of a prefill over its KV tiles. A CTA per (request, KV head,
+// query pair) runs its tiles at a steady rate after a start-up and drain of
+// about five tiles' time; when such CTAs fill few waves of the GPU, the last
+// wave runs part-empty, and splitting every CTA's tiles s ways trades that for
+// s - 1 more start-ups per item and a merge of the partials (written, then
+// read: about 6 MB per tile's time, merge launch included). Both constants are
+// fitted to GB300 timings of the TTFT-sweep batches at s = 1..4. The model picks
+// the s in 1..4 with the least estimated time; shares stay at least 8 tiles.
+int prefill_splits(const lazyattn_pool& p, const lazyattn_batch& b) {
+    const int g = p.d.n_q_heads / p.d.n_kv_heads;
+    if (p.d.dtype != LAZYATTN_BF16 || p.d.head_dim != kD || kRows % g != 0 || b.max_q_len < 1) return 1;
+    const int64_t TQ = kRows / g;
+    const int64_t items = (int64_t)b.num_requests * p.d.n_kv_heads * ((b.max_q_len + TQ - 1) / TQ);
+    const int64_t T = ((int64_t)b.max_entries + kPagesPerTile - 1) / kPagesPerTile;
+    const int64_t sms = p.sm_count > 0 ? p.sm_count : 1;
+    const double merge_bytes_per_tile = 6e6, startup_tiles = 5.0;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int s = 1; s <= 4; ++s) {
+        if (s > 1 && T / s < 8) break;
+        const int64_t ctas = items * s;
+        const double waves = (double)((ctas + sms - 1) / sms);
+        double cost = waves * ((double)((T + s - 1) / s) + startup_tiles);
+        if (s > 1) cost += (double)ctas * kRows * (kD * 4 + 8) * 2.0 / merge_bytes_per_tile;   // written + read
+        if (s == 1 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+size_t prefill_ws_bytes(const lazyattn_pool& p, const lazyattn_batch& b, int splits) {
+    if (splits <= 1) return 0;
+    const int g = p.d.n_q_heads / p.d.n_kv_heads;
+    const size_t TQ = kRows / g;
+    const size_t items = (size_t)b.num_requests * p.d.n_kv_heads * ((b.max_q_len + TQ - 1) / TQ);
+    const size_t slots = items * splits * kRows;
+    return ((slots * kD * sizeof(float) + 255) & ~size_t(255)) + slots * sizeof(float2);
+}
+
 int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const __nv_bfloat16* q,
-                        __nv_bfloat16* out, cudaStream_t stream) {
+                        __nv_bfloat16* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int g = p.d.n_q_heads / p.d.n_kv_heads;
     if (p.d.head_dim != kD || kRows % g != 0) return LAZYATTN_EINVAL;
     if (!p.have_maps) return LAZYATTN_ECUDA;
@@ -904,13 +1028,34 @@ int launch_prefill_bf16(const lazyattn_pool& p, const lazyattn_batch& b, const _
     P.entry_delta = b.entry_delta;
     P.row_blocks = p.have_rmap ? p.d.max_position / kPage : 0;
     const int TQ = kRows / g;
-    dim3 grid((b.max_q_len + TQ - 1) / TQ, p.d.n_kv_heads, b.num_requests);
+    P.qpairs = (b.max_q_len + TQ - 1) / TQ;
+    P.splits = prefill_splits(p, b);
+    P.part_o = nullptr;
+    P.part_ml = nullptr;
+    if (P.splits > 1) {
+        const size_t need = prefill_ws_bytes(p, b, P.splits);
+        if (ws && ws_bytes >= need && !(reinterpret_cast<uintptr_t>(ws) & 255u)) {
+            const size_t slots = (size_t)b.num_requests * p.d.n_kv_heads * P.qpairs * P.splits * kRows;
+            P.part_o = static_cast<float*>(ws);
+            P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
+                                                  ((slots * kD * sizeof(float) + 255) & ~size_t(255)));
+        } else {
+            P.splits = 1;   // no room for the partials: one CTA per item
+        }
+    }
+    dim3 grid(P.qpairs * P.splits, p.d.n_kv_heads, b.num_requests);
     auto kern = prefill_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0,
                                    p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL, p.d.rope_interleaved != 0,
-                                   p.d.position_encoding == LAZYATTN_POS_ALIBI);
+                                   p.d.position_encoding == LAZYATTN_POS_ALIBI, P.splits > 1);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(p.kmap, p.vmap, p.kmap4, p.vmap4, p.kmap8, p.vmap8, p.rmap, p.view(),
                                                  P);
-    return cudaGetLastError() == cudaSuccess ? LAZYATTN_OK : LAZYATTN_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return LAZYATTN_ECUDA;
+    if (P.splits > 1) {
+        prefill_combine_kernel<<<dim3(P.qpairs * p.d.n_kv_heads * b.num_requests, kRows / 16), 256, 0, stream>>>(
+            p.view(), P);
+        if (cudaGetLastError() != cudaSuccess) return LAZYATTN_ECUDA;
+    }
+    return LAZYATTN_OK;
 }
 
 }  // namespace lazyattn

@@ -336,7 +336,10 @@ static int check_batch(const lazyattn_pool* pool, const lazyattn_batch* b, int o
 
 size_t lazyattn_workspace_size(lazyattn_pool_t pool, int32_t op, const lazyattn_batch* batch) {
     if (check_batch(pool, batch, op) != LAZYATTN_OK) return 0;
-    if (op == LAZYATTN_OP_PREFILL) return 256;
+    if (op == LAZYATTN_OP_PREFILL) {
+        const int splits = pool->d.dtype == LAZYATTN_BF16 ? prefill_splits(*pool, *batch) : 1;
+        return splits > 1 ? prefill_ws_bytes(*pool, *batch, splits) : 256;
+    }
     if (op != LAZYATTN_OP_DECODE) return 0;
     if (pool->d.dtype == LAZYATTN_F32) return (size_t)batch->num_requests * sizeof(int32_t) + 256;
     if (batch->decode_plan) return decode_plan_ws_bytes(*pool, *batch->decode_plan);
@@ -351,14 +354,12 @@ int lazyattn_prefill(lazyattn_pool_t pool, const lazyattn_batch* batch, const vo
     if (!q || !out || !aligned16(q) || !aligned16(out)) return LAZYATTN_EINVAL;
     rc = check_device(pool);
     if (rc != LAZYATTN_OK) return rc;
-    (void)workspace;
-    (void)workspace_bytes;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (pool->d.dtype == LAZYATTN_F32)
         return launch_attention_f32(*pool, *batch, static_cast<const float*>(q), static_cast<float*>(out),
                                     nullptr, st);
     return launch_prefill_bf16(*pool, *batch, static_cast<const __nv_bfloat16*>(q),
-                               static_cast<__nv_bfloat16*>(out), st);
+                               static_cast<__nv_bfloat16*>(out), workspace, workspace_bytes, st);
 }
 
 int lazyattn_decode(lazyattn_pool_t pool, const lazyattn_batch* batch, const void* q, const void* k_new,
