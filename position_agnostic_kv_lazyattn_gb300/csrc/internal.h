@@ -190,8 +190,9 @@ struct lazyattn_pool {
     CUtensorMap kmap4, vmap4;          // {D, slot, KV head, page}, boxes of four consecutive pages
     CUtensorMap kmap8, vmap8;          // the same view, boxes of eight consecutive pages
     bool have_rmap = false;            // rmap encoded (position tables of at least 128 rows)
-    CUtensorMap rmap;                  // position table as {2 * (D/2) floats, 16, max_position / 16}:
-                                       // a box holds rows p, p + 16, ..., p + 112 (eight pages' starts)
+    CUtensorMap rmap, rmap4;           // position table as {2 * (D/2) floats, 16, max_position / 16}:
+                                       // a box holds rows p, p + 16, ..., p + 112 (eight pages' starts;
+                                       // rmap4: four pages')
     lazyattn::PoolView view() const;
 };
 

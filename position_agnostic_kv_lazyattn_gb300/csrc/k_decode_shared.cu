@@ -75,14 +75,17 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzled tiles need 1 KB alignment");
 static_assert(2 * kSmemBytes <= 232448, "two CTAs per SM");
 
-struct TileInfo {
+// (written with 16-byte stores, after the tile's copies are issued)
+struct __align__(16) TileInfo {
     int j;                       // tile index, -1: no more tiles
     int page0;                   // page of the tile's first entry
     int consec;                  // pages page0 .. page0 + 3, all with keys: one 4-page box per half
+    int pad;
     int rel[kPagesPerTile];      // run-local position of slot 0 of each page (doc-local: relative offset)
     int n[kPagesPerTile];        // keys in each page (0: none / unusable)
     int y[kPagesPerTile];        // row of the page in the K/V tensor maps (out of range: zero fill)
 };
+static_assert(sizeof(TileInfo) == 4 * 16, "tile info layout (written as four 16-byte words)");
 
 struct SharedParams {
     const uint64_t* entries;
@@ -95,6 +98,7 @@ struct SharedParams {
     int32_t g;
     int32_t oob_row;             // a row index outside the K/V tensor maps: TMA fills zeros
     const int32_t* entry_delta;  // doc-local pools: document offset of each entry
+    int32_t row_blocks;          // rows of the position-table view (max_position / 16); 0: no view
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -170,7 +174,7 @@ template <bool PREROT, bool LOCAL, bool INTER, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_shared_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          const __grid_constant__ CUtensorMap kmap4, const __grid_constant__ CUtensorMap vmap4,
-                         PoolView pv, SharedParams P) {
+                         const __grid_constant__ CUtensorMap rmap4, PoolView pv, SharedParams P) {
     constexpr bool ROT_K = !PREROT && !ALIBI;   // keys rotated here (run-local or relative doc-local)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -295,22 +299,25 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!ok) break;
             if (lane == 0) {
                 TileInfo& info = s_info[k & (kInfoSlots - 1)];
-                int ys[kPagesPerTile];
+                int ys[kPagesPerTile], nn[kPagesPerTile];
 #pragma unroll
                 for (int p = 0; p < kPagesPerTile; ++p) {
                     ys[p] = tn[p] > 0 ? ((int)tpg[p] * Hkv + h) * kPage : P.oob_row;
-                    info.rel[p] = trel[p];
-                    info.n[p] = max(tn[p], 0);
-                    info.y[p] = ys[p];
+                    nn[p] = max(tn[p], 0);
                 }
-                info.j = j;
-                info.page0 = (int)tpg[0];
-                info.consec = consec ? 1 : 0;
-                mbar_arrive(smem_u32(&bar_info[k & (kInfoSlots - 1)]));   // releases the info writes
+                // rows of the position table: one box of its 16-row view when the
+                // four pages start 16 positions apart, else a copy per page
+                bool strided = ROT_K && !LOCAL && P.row_blocks > 0 && trel[0] >= 0 &&
+                               trel[0] / kPage + kPagesPerTile <= P.row_blocks;
+#pragma unroll
+                for (int p = 0; p < kPagesPerTile; ++p) strided = strided && tn[p] > 0 && trel[p] == trel[0] + kPage * p;
                 const uint32_t fb = smem_u32(&bar_kfull[st]);
                 const uint32_t ds = smem_u32(sm + kOffK + st * kKVBytes);
                 const uint32_t bs = smem_u32(sm + kOffBase + st * kBaseBytes);
-                mbar_arrive_expect_tx(fb, kKVBytes + (ROT_K ? kBaseBytes : 0));
+                // copies first (each copy instruction costs this thread tens of
+                // nanoseconds); the stage's own arrival comes after the info
+                // writes, so a consumer that sees the stage full sees the info
+                mbar_expect_tx(fb, kKVBytes + (ROT_K ? kBaseBytes : 0));
                 if (consec) {
                     tma_load_4d(ds, &kmap4, 0, 0, h, (int)tpg[0], fb);
                     tma_load_4d(ds + kKVChunk, &kmap4, 64, 0, h, (int)tpg[0], fb);
@@ -321,13 +328,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                         tma_load_2d(ds + kKVChunk + p * 2048, &kmap, 64, ys[p], fb);
                     }
                 }
-                if (ROT_K) {
+                if (strided) {
+                    tma_load_3d(bs, &rmap4, 0, trel[0] % kPage, trel[0] / kPage, fb);
+                } else if (ROT_K) {
 #pragma unroll
                     for (int p = 0; p < kPagesPerTile; ++p) {
                         const float2* base = pv.rope + (tn[p] > 0 ? (size_t)trel[p] * (kD / 2) : 0);
                         bulk_load(bs + p * 512, base, 512, fb);
                     }
                 }
+                int4* iv = reinterpret_cast<int4*>(&info);
+                iv[0] = make_int4(j, (int)tpg[0], consec ? 1 : 0, 0);
+                iv[1] = make_int4(trel[0], trel[1], trel[2], trel[3]);
+                iv[2] = make_int4(nn[0], nn[1], nn[2], nn[3]);
+                iv[3] = make_int4(ys[0], ys[1], ys[2], ys[3]);
+                mbar_arrive(smem_u32(&bar_info[k & (kInfoSlots - 1)]));   // releases the info writes
+                mbar_arrive(fb);
                 last_k[st] = k;
             }
             ++k;
@@ -795,8 +811,8 @@ __global__ void __launch_bounds__(128)
                       pack_bf2(a[4] * inv, a[5] * inv), pack_bf2(a[6] * inv, a[7] * inv));
 }
 
-using SharedKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, PoolView,
-                              SharedParams);
+using SharedKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                              const CUtensorMap, PoolView, SharedParams);
 
 SharedKernel shared_kernel_for(bool prerot, bool local, bool inter, bool alibi) {
     if (alibi) return decode_shared_kernel<false, false, false, true>;
@@ -852,13 +868,13 @@ int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const 
     P.g = p.d.n_q_heads / p.d.n_kv_heads;
     P.oob_row = (int32_t)((uint64_t)p.d.num_pages * (uint64_t)p.d.n_kv_heads * kPage);
     P.entry_delta = b.entry_delta;
+    P.row_blocks = p.have_rmap ? p.d.max_position / kPage : 0;
     auto kern = shared_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0, p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL,
                                   p.d.rope_interleaved != 0, p.d.position_encoding == LAZYATTN_POS_ALIBI);
     if (plan.num_units > 0) {
         dim3 grid(plan.num_units, p.d.n_kv_heads);
-        if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.kmap4, p.vmap4, p.view(),
-                             P) !=
-            cudaSuccess)
+        if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.kmap4, p.vmap4, p.rmap4,
+                             p.view(), P) != cudaSuccess)
             return LAZYATTN_ECUDA;
     }
     const int32_t* pbase = reinterpret_cast<const int32_t*>(img + plan.pbase_off);

@@ -48,14 +48,15 @@ bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* b
 
 // The position table (float2 (cos, sin) rows of D/2 frequencies, one row per
 // position) as a 3-D fp32 tensor {D, 16, max_position / 16} (strides 4 B,
-// 2 D B, 32 D B): a box {D, 1, 8} at (0, t % 16, t / 16) holds the rows of
-// positions t, t + 16, ..., t + 112, i.e. the start rows of eight pages that
-// follow each other at consecutive positions. Positions past the last whole
+// 2 D B, 32 D B): a box {D, 1, pages} at (0, t % 16, t / 16) holds the rows of
+// positions t, t + 16, ..., i.e. the start rows of `pages` pages that follow
+// each other at consecutive positions. Positions past the last whole
 // block of 16 are outside the view (callers copy those rows one by one).
-bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, int32_t max_position, int d) {
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, int32_t max_position, int d,
+                 uint32_t pages) {
     cuuint64_t gdim[3] = {(cuuint64_t)d, (cuuint64_t)kPage, (cuuint64_t)(max_position / kPage)};
     cuuint64_t gstride[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * kPage};
-    cuuint32_t box[3] = {(cuuint32_t)d, 1, 8};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, pages};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -79,7 +80,8 @@ bool encode_pool_maps(lazyattn_pool& p) {
     if (!encode_run(enc, &p.kmap4, p.d.k_pool, np, hkv, d, 4) || !encode_run(enc, &p.vmap4, p.d.v_pool, np, hkv, d, 4) ||
         !encode_run(enc, &p.kmap8, p.d.k_pool, np, hkv, d, 8) || !encode_run(enc, &p.vmap8, p.d.v_pool, np, hkv, d, 8))
         return false;
-    p.have_rmap = p.d.max_position >= 8 * kPage && encode_rows(enc, &p.rmap, p.d.rope_table, p.d.max_position, d);
+    p.have_rmap = p.d.max_position >= 8 * kPage && encode_rows(enc, &p.rmap, p.d.rope_table, p.d.max_position, d, 8) &&
+                  encode_rows(enc, &p.rmap4, p.d.rope_table, p.d.max_position, d, 4);
     p.have_maps = true;
     return true;
 }
