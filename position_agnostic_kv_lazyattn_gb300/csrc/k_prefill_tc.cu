@@ -652,35 +652,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float sc = kLog2e * pv.qk_scale;
             const __nv_bfloat16* qp_ = P.q + ((size_t)(q0 + tok) * Hq + (size_t)h * g + jh) * kD;
             const float* cs = reinterpret_cast<const float*>(pv.rope + (size_t)(row_valid ? m_row : 0) * (kD / 2));
-#pragma unroll 2
-            for (int u = 0; u < 8; ++u) {
-                uint4 w1 = make_uint4(0, 0, 0, 0), w2 = w1;
-                if (row_valid) {
-                    float x1[8], x2[8];
-                    uint4 a = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u : 8 * u)));
-                    uint4 b = __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u + 8 : 64 + 8 * u)));
-                    if (INTER) deinterleave16(a, b, a, b);
-                    unpack8(a, x1);
-                    unpack8(b, x2);
-                    float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
+            // The row's position-table line (512 B) is fetched into L1 while the
+            // q words load; each half of the row's dims loads its q words together.
+            if (!ALIBI && row_valid) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) n2 = fmaxf(n2, fmaf(x1[v], x1[v], x2[v] * x2[v]));
-                    if (!(n2 * sc * sc <= kMaxPairNorm2)) record_error(pv.status, LAZYATTN_ERANGE);
-                    const float4* c4 = reinterpret_cast<const float4*>(cs + 16 * u);
+                for (int l = 0; l < 4; ++l) asm volatile("prefetch.global.L1 [%0];" ::"l"(cs + 32 * l));
+            }
+#pragma unroll 1
+            for (int h4 = 0; h4 < 2; ++h4) {
+                uint4 qa[4], qb[4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const float4 f = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(c4 + v);
-                        const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
-                        x1[2 * v] = (a0 * f.x - z0 * f.y) * sc;
-                        x2[2 * v] = (a0 * f.y + z0 * f.x) * sc;
-                        x1[2 * v + 1] = (a1 * f.z - z1 * f.w) * sc;
-                        x2[2 * v + 1] = (a1 * f.w + z1 * f.z) * sc;
-                    }
-                    w1 = pack8_h(x1);
-                    w2 = pack8_h(x2);
+                for (int i = 0; i < 4; ++i) {
+                    const int u = 4 * h4 + i;
+                    qa[i] = row_valid ? __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u : 8 * u)))
+                                      : make_uint4(0, 0, 0, 0);
+                    qb[i] = row_valid ? __ldg(reinterpret_cast<const uint4*>(qp_ + (INTER ? 16 * u + 8 : 64 + 8 * u)))
+                                      : make_uint4(0, 0, 0, 0);
                 }
-                *reinterpret_cast<uint4*>(qsm + sw128_offset(trow, u)) = w1;
-                *reinterpret_cast<uint4*>(qsm + kQChunk + sw128_offset(trow, u)) = w2;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int u = 4 * h4 + i;
+                    uint4 w1 = make_uint4(0, 0, 0, 0), w2 = w1;
+                    if (row_valid) {
+                        float x1[8], x2[8];
+                        uint4 a = qa[i], b = qb[i];
+                        if (INTER) deinterleave16(a, b, a, b);
+                        unpack8(a, x1);
+                        unpack8(b, x2);
+                        float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) n2 = fmaxf(n2, fmaf(x1[v], x1[v], x2[v] * x2[v]));
+                        if (!(n2 * sc * sc <= kMaxPairNorm2)) record_error(pv.status, LAZYATTN_ERANGE);
+                        const float4* c4 = reinterpret_cast<const float4*>(cs + 16 * u);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 f = ALIBI ? make_float4(1.f, 0.f, 1.f, 0.f) : __ldg(c4 + v);
+                            const float a0 = x1[2 * v], z0 = x2[2 * v], a1 = x1[2 * v + 1], z1 = x2[2 * v + 1];
+                            x1[2 * v] = (a0 * f.x - z0 * f.y) * sc;
+                            x2[2 * v] = (a0 * f.y + z0 * f.x) * sc;
+                            x1[2 * v + 1] = (a1 * f.z - z1 * f.w) * sc;
+                            x2[2 * v + 1] = (a1 * f.w + z1 * f.z) * sc;
+                        }
+                        w1 = pack8_h(x1);
+                        w2 = pack8_h(x2);
+                    }
+                    *reinterpret_cast<uint4*>(qsm + sw128_offset(trow, u)) = w1;
+                    *reinterpret_cast<uint4*>(qsm + kQChunk + sw128_offset(trow, u)) = w2;
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
