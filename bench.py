@@ -70,10 +70,10 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    # decode call = decode_shared 4,636,032,768 + 72,134,144; combine 70,302,208 + 229,120;
-    # append 299,520 (read + write bytes); prefill 8,542,410,752 + 260,228,096
-    ("llama3_70b", "decode"): (4778997760.0, "b1006cea44273475"),
-    ("llama3_70b", "prefill"): (8802638848.0, "492e39bcf0b528b3"),
+    # decode call = decode_shared 4,635,946,325 + 72,088,917; combine 70,300,501 + 4,011;
+    # append 297,557 (read + write bytes, mean of three calls); prefill 8,636,470,272 + 260,794,880
+    ("llama3_70b", "decode"): (4778637312.0, "4b0fef217048ee08"),
+    ("llama3_70b", "prefill"): (8897265152.0, "4003343b0cf0199c"),
 }
 
 
