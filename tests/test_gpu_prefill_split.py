@@ -13,7 +13,10 @@ second kernel. These tests check:
 * the same batch without a workspace, and with one too small for the partials
   (one CTA per item, no merge): the same outputs within the same bounds;
 * the TTFT sweep's 20- and 40-document batches (where the split is chosen) in
-  the launch configuration the benchmark times.
+  the launch configuration the benchmark times;
+* every other instantiation of the split kernel: doc-local keys, ALiBi, the
+  materialising baseline's pre-rotated pages, interleaved RoPE pairs (with
+  position-free and doc-local keys).
 """
 import numpy as np
 import pytest
@@ -111,4 +114,46 @@ def test_ttft_sweep_split(L, name):
     ref = Reference(cfg)
     errs = [compare(got[r], ref.prefill(r), "bf16") for r in (0, 13, 31)]
     print("%s split prefill worst max-abs %.3e rel-L2 %.3e" % (name, max(e[0] for e in errs), max(e[1] for e in errs)))
+    assert env.pool.device_status() == 0
+
+
+@pytest.mark.parametrize("mode", ["doc_local", "alibi", "materialised", "interleaved", "doc_local+interleaved"])
+def test_split_layouts(L, mode):
+    """Every instantiation of the split kernel: two long requests of the
+    40-document sweep (one wave of CTAs, so the tiles split four ways) in each
+    pool layout and position encoding, against the oracle's attention for it."""
+    cfg = workload.CONFIGS["ttft_sweep_40"]
+    reqs = [0, 5]
+    kw = {}
+    if "doc_local" in mode:
+        kw["key_storage"] = "doc_local"
+    if mode == "alibi":
+        kw["position_encoding"] = "alibi"
+    if "interleaved" in mode:
+        kw["rope_interleaved"] = True
+    env = workload.device.setup(cfg, requests=reqs, all_docs=False, baseline=(mode == "materialised"), **kw)
+    batch = env.batch
+    if mode == "materialised":
+        b = env.batch
+        dst = (b.entries_host & ~np.uint64(0xFFFFFFFF)) | np.array(env.pool.alloc_pages(len(b.entries_host)), np.uint64)
+        L.lazyattn_materialize(env.pool.handle, b.c, torch.from_numpy(dst.view(np.int64).copy()).cuda())
+        batch = b.with_entries(dst, L.LAZYATTN_KEYS_PREROTATED)
+    ws, nbytes = _workspace(L, env.pool, batch)
+    assert nbytes > 256
+    out = torch.full((batch.total_q, cfg.n_q_heads, cfg.head_dim), float("nan"), dtype=env.pool.tdtype, device="cuda")
+    L.lazyattn_prefill(env.pool.handle, batch.c, env.q, out, ws, nbytes)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().reshape(len(reqs), cfg.q_len, cfg.n_q_heads, cfg.head_dim)
+    ref = Reference(cfg)
+    if mode == "alibi":
+        positional = oracle.AlibiSpec()
+    elif "interleaved" in mode:
+        positional = oracle.RopeSpec(cfg.rope_theta, "default", 1.0, 0, 0.0, 0.0, "interleaved")
+    else:
+        positional = cfg.rope_theta
+    errs = []
+    for i, r in enumerate(reqs):
+        q, kq, vq = ref.qseg(r)
+        errs.append(compare(got[i], oracle.prefill_request(ref.ctx(r), q, kq, vq, positional), "bf16"))
+    print("%s split prefill worst max-abs %.3e rel-L2 %.3e" % (mode, max(e[0] for e in errs), max(e[1] for e in errs)))
     assert env.pool.device_status() == 0
