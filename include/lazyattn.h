@@ -106,7 +106,11 @@ typedef enum lazyattn_dtype { LAZYATTN_F32 = 0, LAZYATTN_BF16 = 1 } lazyattn_dty
  *   rope_theta    RoPE base (> 0), frequencies theta^(-2i/D), i < D/2
  *   max_position  the position table covers logical positions [0, max_position)
  *   k_pool/v_pool [num_pages][n_kv_heads][16][head_dim]
- *   rope_table    float2 [max_position][head_dim/2]; filled by lazyattn_pool_create
+ *   rope_table    lazyattn_rope_table_bytes(head_dim, max_position) bytes, filled by
+ *                 lazyattn_pool_create: float2 [max_position][head_dim/2] (cos, sin) of
+ *                 each frequency, then the same values as float4 [max_position][head_dim/4]
+ *                 (cos f, cos f+1, sin f, sin f+1) for even f (the per-page rows the
+ *                 bf16 kernels stage in shared memory, paired for two-lane arithmetic)
  *   status_word   one int32 in device memory, zeroed by lazyattn_pool_create; kernels
  *                 record the first device-side error there
  *   rope_scaling  LAZYATTN_ROPE_* below (0: plain RoPE; the fields after it are then ignored)
@@ -237,7 +241,8 @@ const char* lazyattn_status_string(int status);
  * fields are masked to their width (host helper; no validation). */
 uint64_t lazyattn_pack_entry(int32_t page, int32_t start, int32_t nvalid, int32_t writable);
 
-/* Bytes of the position table for head_dim and max_position (host helper). */
+/* Bytes of the position table for head_dim and max_position (host helper):
+ * both layouts described under lazyattn_pool_desc.rope_table. */
 size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position);
 
 /* Create a pool over caller-owned buffers (§3 "Problem statement": one store of

@@ -58,6 +58,7 @@ struct PoolView {
     void* k_pool;
     void* v_pool;
     const float2* rope;   // [max_position][D/2] (cos, sin)
+    const float4* rope_pair;   // [max_position][D/4] (cos f, cos f+1, sin f, sin f+1), f even
     int32_t* status;
     int32_t num_pages;
     int32_t max_position;
@@ -190,7 +191,7 @@ struct lazyattn_pool {
     CUtensorMap kmap4, vmap4;          // {D, slot, KV head, page}, boxes of four consecutive pages
     CUtensorMap kmap8, vmap8;          // the same view, boxes of eight consecutive pages
     bool have_rmap = false;            // rmap encoded (position tables of at least 128 rows)
-    CUtensorMap rmap, rmap4;           // position table as {2 * (D/2) floats, 16, max_position / 16}:
+    CUtensorMap rmap, rmap4;           // paired position table as {D floats, 16, max_position / 16}:
                                        // a box holds rows p, p + 16, ..., p + 112 (eight pages' starts;
                                        // rmap4: four pages')
     lazyattn::PoolView view() const;

@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 } else if (ROT_K) {
 #pragma unroll
                     for (int p = 0; p < kPagesPerTile; ++p) {
-                        const float2* base = pv.rope + (tn[p] > 0 ? (size_t)trel[p] * (kD / 2) : 0);
+                        const float4* base = pv.rope_pair + (tn[p] > 0 ? (size_t)trel[p] * (kD / 4) : 0);
                         bulk_load(bs + p * 512, base, 512, fb);
                     }
                 }
@@ -480,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
         float2 cs2[4], sn2[4];   // (cos, sin)(slot * theta_f) for f = 8u + 2v, 8u + 2v + 1
         if (ROT_K && !LOCAL) {
-            const float4* t4 = reinterpret_cast<const float4*>(pv.rope + (size_t)slot * (kD / 2) + 8 * u);
+            const float4* t4 = pv.rope_pair + (size_t)slot * (kD / 4) + 4 * u;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
-                cs2[v] = make_float2(f.x, f.z);
-                sn2[v] = make_float2(f.y, f.w);
+                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 1.f, 0.f, 0.f);
+                cs2[v] = make_float2(f.x, f.y);
+                sn2[v] = make_float2(f.z, f.w);
             }
         }
         // One thread polls the stage's barrier; the named barrier releases the
@@ -530,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1
-                            const float4 bv = b4[v];
-                            float2 c = make_float2(bv.x, bv.z), s = make_float2(bv.y, bv.w);
+                            const float4 bv = b4[v];   // (cos f, cos f+1, sin f, sin f+1)
+                            float2 c = make_float2(bv.x, bv.y), s = make_float2(bv.z, bv.w);
                             if (!LOCAL) {   // angle of rel + slot
                                 const float2 cc = f2_fma(c, cs2[v], f2_mul(f2_neg(s), sn2[v]));
                                 s = f2_fma(s, cs2[v], f2_mul(c, sn2[v]));

@@ -160,6 +160,33 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
     return o;
 }
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "mul.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "sub.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\tmov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
 // Entry check shared by every role so that all of them agree on which slots
 // hold keys: page in range and positions inside the table.
 __device__ __forceinline__ int usable_tokens(const PoolView& pv, uint64_t e) {
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int p = 0; p < kPagesPerTile; ++p) {
                             const int rowpos = LOCAL ? curd[p] : ss[p];   // position of the page's rotation
-                            const float2* base = pv.rope + (n[p] > 0 ? (size_t)rowpos * (kD / 2) : 0);
+                            const float4* base = pv.rope_pair + (n[p] > 0 ? (size_t)rowpos * (kD / 4) : 0);
                             bulk_load(bs + p * 512, base, 512, fb);
                         }
                     }
@@ -527,16 +554,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half and 64+8u.. of the second half of every key row with this slot.
         const int rt = threadIdx.x - 384;
         const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
-        float cs[8], sn[8];   // (cos, sin)(slot * theta_f), f = 8u + 0..7
+        // (cos, sin, -sin)(slot * theta_f) for f = 8u + 2v, 8u + 2v + 1, as lane pairs
+        float2 cs2[4], sn2[4], nsn2[4];
         if (!PREROT && !ALIBI && !LOCAL) {
-            const float4* t4 = reinterpret_cast<const float4*>(pv.rope + (size_t)slot * (kD / 2) + 8 * u);
+            const float4* t4 = pv.rope_pair + (size_t)slot * (kD / 4) + 4 * u;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
-                cs[2 * v] = f.x;
-                sn[2 * v] = f.y;
-                cs[2 * v + 1] = f.z;
-                sn[2 * v + 1] = f.w;
+                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 1.f, 0.f, 0.f);
+                cs2[v] = make_float2(f.x, f.y);
+                sn2[v] = make_float2(f.z, f.w);
+                nsn2[v] = make_float2(-f.z, -f.w);
             }
         }
         // One thread polls the stage's barrier and a named barrier releases the
@@ -590,21 +617,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unpack8(w1[q], x1);
                     unpack8(w2[q], x2);
                     if (!PREROT && !ALIBI) {
+                        // the page's row holds (cos f, cos f+1, sin f, sin f+1) groups
                         const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1
+                        for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1, two lanes
                             const float4 b = b4[v];
-#pragma unroll
-                            for (int w = 0; w < 2; ++w) {
-                                const int f = 2 * v + w;
-                                const float cb = w ? b.z : b.x, sb = w ? b.w : b.y;
-                                // LOCAL: the page's one relative rotation; else start + slot
-                                const float c = LOCAL ? cb : cb * cs[f] - sb * sn[f];
-                                const float s_ = LOCAL ? sb : sb * cs[f] + cb * sn[f];
-                                const float a = x1[f], z = x2[f];
-                                x1[f] = a * c - z * s_;
-                                x2[f] = a * s_ + z * c;
+                            float2 c = make_float2(b.x, b.y), s_ = make_float2(b.z, b.w);
+                            if (!LOCAL) {   // angle of start + slot; LOCAL: the page's one relative rotation
+                                const float2 cc = f2_fma(c, cs2[v], f2_mul(s_, nsn2[v]));
+                                s_ = f2_fma(s_, cs2[v], f2_mul(c, sn2[v]));
+                                c = cc;
                             }
+                            const float2 a = make_float2(x1[2 * v], x1[2 * v + 1]);
+                            const float2 z = make_float2(x2[2 * v], x2[2 * v + 1]);
+                            const float2 r1 = f2_sub(f2_mul(a, c), f2_mul(z, s_));
+                            const float2 r2 = f2_fma(a, s_, f2_mul(z, c));
+                            x1[2 * v] = r1.x;
+                            x1[2 * v + 1] = r1.y;
+                            x2[2 * v] = r2.x;
+                            x2[2 * v + 1] = r2.y;
                         }
                     }
                     // no key in this slot: zero K so that its scores stay finite

@@ -19,6 +19,7 @@ lazyattn::PoolView lazyattn_pool::view() const {
     v.k_pool = d.k_pool;
     v.v_pool = d.v_pool;
     v.rope = static_cast<const float2*>(d.rope_table);
+    v.rope_pair = reinterpret_cast<const float4*>(v.rope + (size_t)d.max_position * (size_t)(d.head_dim / 2));
     v.status = d.status_word;
     v.num_pages = d.num_pages;
     v.max_position = d.max_position;
@@ -63,7 +64,7 @@ uint64_t lazyattn_pack_entry(int32_t page, int32_t start, int32_t nvalid, int32_
 
 size_t lazyattn_rope_table_bytes(int32_t head_dim, int32_t max_position) {
     if (head_dim <= 0 || max_position <= 0) return 0;
-    return (size_t)max_position * (size_t)(head_dim / 2) * sizeof(float2);
+    return 2 * (size_t)max_position * (size_t)(head_dim / 2) * sizeof(float2);   // two layouts
 }
 
 // theta_i, i < D/2, of the pool's RoPE variant (fp64), and the logit scale.
@@ -182,7 +183,7 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
     std::vector<float2> tab;
     std::vector<double> inv;
     try {
-        tab.resize((size_t)d.max_position * (size_t)half);
+        tab.resize(2 * (size_t)d.max_position * (size_t)half);   // (cos, sin) rows, then the paired rows
         inv.resize((size_t)half);
     } catch (...) {
         delete p;
@@ -196,6 +197,12 @@ int lazyattn_pool_create(const lazyattn_pool_desc* desc, void* stream, lazyattn_
             for (int i = 0; i < half; ++i) {
                 const double a = (double)pos * inv[i];
                 row[i] = make_float2((float)cos(a), (float)sin(a));
+            }
+            // the same row as (cos f, cos f+1, sin f, sin f+1) groups, f even
+            float2* pair = &tab[((size_t)d.max_position + (size_t)pos) * half];
+            for (int i = 0; i < half; i += 2) {
+                pair[i] = make_float2(row[i].x, row[i + 1].x);
+                pair[i + 1] = make_float2(row[i].y, row[i + 1].y);
             }
         }
     };

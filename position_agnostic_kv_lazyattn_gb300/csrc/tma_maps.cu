@@ -46,8 +46,8 @@ bool encode_run(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The position table (float2 (cos, sin) rows of D/2 frequencies, one row per
-// position) as a 3-D fp32 tensor {D, 16, max_position / 16} (strides 4 B,
+// The paired position table (rows of D floats, (cos f, cos f+1, sin f, sin f+1)
+// for even f, one row per position) as a 3-D fp32 tensor {D, 16, max_position / 16} (strides 4 B,
 // 2 D B, 32 D B): a box {D, 1, pages} at (0, t % 16, t / 16) holds the rows of
 // positions t, t + 16, ..., i.e. the start rows of `pages` pages that follow
 // each other at consecutive positions. Positions past the last whole
@@ -80,8 +80,9 @@ bool encode_pool_maps(lazyattn_pool& p) {
     if (!encode_run(enc, &p.kmap4, p.d.k_pool, np, hkv, d, 4) || !encode_run(enc, &p.vmap4, p.d.v_pool, np, hkv, d, 4) ||
         !encode_run(enc, &p.kmap8, p.d.k_pool, np, hkv, d, 8) || !encode_run(enc, &p.vmap8, p.d.v_pool, np, hkv, d, 8))
         return false;
-    p.have_rmap = p.d.max_position >= 8 * kPage && encode_rows(enc, &p.rmap, p.d.rope_table, p.d.max_position, d, 8) &&
-                  encode_rows(enc, &p.rmap4, p.d.rope_table, p.d.max_position, d, 4);
+    void* pair = const_cast<float4*>(p.view().rope_pair);
+    p.have_rmap = p.d.max_position >= 8 * kPage && encode_rows(enc, &p.rmap, pair, p.d.max_position, d, 8) &&
+                  encode_rows(enc, &p.rmap4, pair, p.d.max_position, d, 4);
     p.have_maps = true;
     return true;
 }

@@ -52,7 +52,8 @@ static int host_checks(void) {
     /* status strings are never NULL */
     for (int s = 1; s >= -9; --s)
         if (!lazyattn_status_string(s)) FAIL("status string %d", s);
-    if (lazyattn_rope_table_bytes(128, 1000) != (size_t)1000 * 64 * 8) FAIL("rope_table_bytes");
+    /* (cos, sin) rows, then the same rows paired for two-lane arithmetic */
+    if (lazyattn_rope_table_bytes(128, 1000) != (size_t)2 * 1000 * 64 * 8) FAIL("rope_table_bytes");
     /* invalid descriptors are rejected before any CUDA call */
     lazyattn_pool_desc d;
     memset(&d, 0, sizeof d);

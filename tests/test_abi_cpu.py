@@ -70,7 +70,7 @@ def test_binding_constants_match_the_header(L):
 
 
 def test_rope_table_bytes(L):
-    assert L.lazyattn_rope_table_bytes(128, 1000) == 1000 * 64 * 8
+    assert L.lazyattn_rope_table_bytes(128, 1000) == 2 * 1000 * 64 * 8   # (cos, sin) rows + paired rows
     assert L.lazyattn_rope_table_bytes(0, 10) == 0
 
 
