@@ -92,6 +92,8 @@ struct __align__(16) TileInfo {
     int start[kPagesPerTile];     // logical position of slot 0 of each page
     int n[kPagesPerTile];         // keys in each page (0: none / unusable)
     int y[kPagesPerTile];         // row of the page in the K/V tensor maps (out of range: zero fill)
+    int full_from;                // every page full: rows at positions >= this see every key; else INT_MAX
+    int pad[3];
 };
 
 struct PrefillParams {
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap kmap8, const __grid_constant__ CUtensorMap vmap8,
                       const __grid_constant__ CUtensorMap rmap, PoolView pv, PrefillParams P) {
     constexpr bool ROT = !PREROT && !ALIBI;   // K rotated here: the pages' position-table rows are loaded
-    static_assert(sizeof(TileInfo) == 7 * 16, "tile info layout (written as seven 16-byte words)");
+    static_assert(sizeof(TileInfo) == 8 * 16, "tile info layout (written as eight 16-byte words)");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -400,6 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     iv[4] = make_int4(nn[4], nn[5], nn[6], nn[7]);
                     iv[5] = make_int4(ys[0], ys[1], ys[2], ys[3]);
                     iv[6] = make_int4(ys[4], ys[5], ys[6], ys[7]);
+                    int full_from = 0;
+#pragma unroll
+                    for (int p = 0; p < kPagesPerTile; ++p)
+                        full_from = nn[p] == kPage ? max(full_from, ss[p] + kPage - 1) : INT_MAX;
+                    iv[7] = make_int4(full_from, 0, 0, 0);
                     mbar_arrive(ib);   // releases the info writes to the other roles
                     mbar_arrive(fb);
                     if (bad) record_error(pv.status, LAZYATTN_ERANGE);
@@ -748,11 +755,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const TileInfo& info = s_info[is];
             if (info.j < 0) break;
+            // a warp whose rows all see every key of the tile skips the masking
+            const bool wfull = __all_sync(0xffffffffu, row_valid && m_row >= info.full_from);
             // visibility of the tile's keys to this row: bit i of visN is key
             // 32N + i (pages 2N and 2N+1 hold slots [0, lim) of their 16)
-            uint32_t vis[4];
+            uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
+            for (int w = 0; w < 4 && !wfull; ++w) {
                 uint32_t bits = 0;
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
@@ -762,9 +771,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 vis[w] = bits;
             }
-            const bool full = (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu;
-            // a warp whose rows all see every key of the tile skips the masking
-            const bool wfull = __all_sync(0xffffffffu, full);
             ok = mbar_wait(smem_u32(&bar_sfull[qi]), k & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
