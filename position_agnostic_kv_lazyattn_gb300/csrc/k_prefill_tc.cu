@@ -30,10 +30,11 @@
 //                 positions, online softmax in the log2 domain with lazy
 //                 rescaling of O (only when the row max grows by > 8); P is
 //                 written as bf16 over the first 64 columns of its own S
-//   warps 12-15   K rotation: thread = (slot, 8 frequencies), so the slot's
-//                 (cos, sin)(slot * theta) stay in registers; per page the
-//                 start's row from shared memory; cos/sin(start + slot) by angle
-//                 addition; written back in place as fp16
+//   warps 12-15   K rotation: thread = (page, 4 frequencies) over the page's
+//                 16 keys; the angle of slot 0 is the page's row of the position
+//                 table (read once per tile from shared memory), each next
+//                 slot's angle the previous one turned by theta (angle addition
+//                 in registers); written back in place as fp16
 // TMEM: S_0, S_1, O_0, O_1, 128 columns each. P_i aliases S_i: the MMA that
 // next overwrites S_i is issued after the PV MMA that reads P_i, and
 // tcgen05.mma operations of one thread execute in issue order. The same order
@@ -557,20 +558,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ K rotation
-        // Thread = (slot, group u of 8 frequencies): dims 8u..8u+7 of the first
-        // half and 64+8u.. of the second half of every key row with this slot.
+        // Thread = (page p, group u of 4 frequencies): dims 4u..4u+3 of both
+        // halves of the page's 16 key rows. The angle of slot 0 is the page's
+        // row of the (paired) position table; each next slot's angle is the
+        // previous one turned by theta (angle addition in registers), so a
+        // thread reads its page's row once per tile.
         const int rt = threadIdx.x - 384;
-        const int u = 2 * (rt >> 5) + (lane >> 4), slot = lane & 15;
-        // (cos, sin, -sin)(slot * theta_f) for f = 8u + 2v, 8u + 2v + 1, as lane pairs
-        float2 cs2[4], sn2[4], nsn2[4];
+        const int p = rt >> 4, u = rt & 15;
+        // (cos, sin, -sin)(theta_f) for f = 4u, 4u+1 and 4u+2, 4u+3, as lane pairs
+        float2 c1[2], s1[2], ns1[2];
         if (!PREROT && !ALIBI && !LOCAL) {
-            const float4* t4 = pv.rope_pair + (size_t)slot * (kD / 4) + 4 * u;
+            const float4* t4 = pv.rope_pair + (size_t)(kD / 4) + 2 * u;   // position 1
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const float4 f = slot < pv.max_position ? __ldg(t4 + v) : make_float4(1.f, 1.f, 0.f, 0.f);
-                cs2[v] = make_float2(f.x, f.y);
-                sn2[v] = make_float2(f.z, f.w);
-                nsn2[v] = make_float2(-f.z, -f.w);
+            for (int v = 0; v < 2; ++v) {
+                const float4 f = pv.max_position > 1 ? __ldg(t4 + v) : make_float4(1.f, 1.f, 0.f, 0.f);
+                c1[v] = make_float2(f.x, f.y);
+                s1[v] = make_float2(f.z, f.w);
+                ns1[v] = make_float2(-f.z, -f.w);
             }
         }
         // One thread polls the stage's barrier and a named barrier releases the
@@ -600,61 +604,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&bar_kready[st]));
                 break;
             }
-            int n[kPagesPerTile];
+            const int np = info.n[p];
+            // key row 16p + s, dims 4u..4u+3: 8 bytes in 16-byte unit u / 2 of each half
+            uint8_t* kb = sm + kOffK + st * kKVBytes + (2 * p) * 1024 + (u & 1) * 8;
+            float2 C[2], S[2];
+            if (!PREROT && !ALIBI) {
+                const float4* b4 = reinterpret_cast<const float4*>(sm + kOffBase + st * kBaseBytes + p * 512) + 2 * u;
 #pragma unroll
-            for (int p = 0; p < kPagesPerTile; ++p) n[p] = info.n[p];
-            uint8_t* kb = sm + kOffK + st * kKVBytes;
-            const uint8_t* bb = sm + kOffBase + st * kBaseBytes + u * 64;
-            // Two pages at a time: both pages' loads before the first store,
-            // so that their latencies overlap (the loop body stays compact:
-            // the four roles' code shares the instruction caches).
-#pragma unroll 1
-            for (int h4 = 0; h4 < 8 / 2; ++h4) {
-                uint4 w1[2], w2[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int kr = (2 * h4 + q) * kPage + slot;
-                    w1[q] = *reinterpret_cast<const uint4*>(kb + sw128_offset(kr, u));
-                    w2[q] = *reinterpret_cast<const uint4*>(kb + kKVChunk + sw128_offset(kr, u));
+                for (int v = 0; v < 2; ++v) {
+                    const float4 b = b4[v];   // (cos f, cos f+1, sin f, sin f+1)
+                    C[v] = make_float2(b.x, b.y);
+                    S[v] = make_float2(b.z, b.w);
                 }
+            }
+#pragma unroll 1
+            for (int s8 = 0; s8 < 2; ++s8) {
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int p = 2 * h4 + q;
-                    float x1[8], x2[8];
-                    unpack8(w1[q], x1);
-                    unpack8(w2[q], x2);
-                    if (!PREROT && !ALIBI) {
-                        // the page's row holds (cos f, cos f+1, sin f, sin f+1) groups
-                        const float4* b4 = reinterpret_cast<const float4*>(bb + p * 512);
+                for (int j = 0; j < 8; ++j) {
+                    const int s = 8 * s8 + j;
+                    uint2* p1 = reinterpret_cast<uint2*>(kb + s8 * 1024 + j * 128 + (((u >> 1) ^ j) << 4));
+                    uint2* p2 = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p1) + kKVChunk);
+                    uint2 w1 = make_uint2(0, 0), w2 = w1;
+                    if (s < np) {   // no key in this slot: zero K so that its scores stay finite
+                        const uint2 a = *p1, z = *p2;
+                        float x1[4] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y)};
+                        float x2[4] = {bf_lo(z.x), bf_hi(z.x), bf_lo(z.y), bf_hi(z.y)};
+                        if (!PREROT && !ALIBI) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {   // frequencies 8u + 2v, 8u + 2v + 1, two lanes
-                            const float4 b = b4[v];
-                            float2 c = make_float2(b.x, b.y), s_ = make_float2(b.z, b.w);
-                            if (!LOCAL) {   // angle of start + slot; LOCAL: the page's one relative rotation
-                                const float2 cc = f2_fma(c, cs2[v], f2_mul(s_, nsn2[v]));
-                                s_ = f2_fma(s_, cs2[v], f2_mul(c, sn2[v]));
-                                c = cc;
+                            for (int v = 0; v < 2; ++v) {
+                                const float2 xa = make_float2(x1[2 * v], x1[2 * v + 1]);
+                                const float2 xz = make_float2(x2[2 * v], x2[2 * v + 1]);
+                                const float2 r1 = f2_sub(f2_mul(xa, C[v]), f2_mul(xz, S[v]));
+                                const float2 r2 = f2_fma(xa, S[v], f2_mul(xz, C[v]));
+                                x1[2 * v] = r1.x;
+                                x1[2 * v + 1] = r1.y;
+                                x2[2 * v] = r2.x;
+                                x2[2 * v + 1] = r2.y;
                             }
-                            const float2 a = make_float2(x1[2 * v], x1[2 * v + 1]);
-                            const float2 z = make_float2(x2[2 * v], x2[2 * v + 1]);
-                            const float2 r1 = f2_sub(f2_mul(a, c), f2_mul(z, s_));
-                            const float2 r2 = f2_fma(a, s_, f2_mul(z, c));
-                            x1[2 * v] = r1.x;
-                            x1[2 * v + 1] = r1.y;
-                            x2[2 * v] = r2.x;
-                            x2[2 * v + 1] = r2.y;
+                        }
+                        w1 = make_uint2(pack_h2(x1[0], x1[1]), pack_h2(x1[2], x1[3]));
+                        w2 = make_uint2(pack_h2(x2[0], x2[1]), pack_h2(x2[2], x2[3]));
+                    }
+                    *p1 = w1;
+                    *p2 = w2;
+                    if (!PREROT && !ALIBI && !LOCAL) {   // next slot: angle + theta
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const float2 cc = f2_fma(C[v], c1[v], f2_mul(S[v], ns1[v]));
+                            S[v] = f2_fma(S[v], c1[v], f2_mul(C[v], s1[v]));
+                            C[v] = cc;
                         }
                     }
-                    // no key in this slot: zero K so that its scores stay finite
-                    const bool key = slot < n[p];
-                    w1[q] = key ? pack8_h(x1) : make_uint4(0, 0, 0, 0);
-                    w2[q] = key ? pack8_h(x2) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int kr = (2 * h4 + q) * kPage + slot;
-                    *reinterpret_cast<uint4*>(kb + sw128_offset(kr, u)) = w1[q];
-                    *reinterpret_cast<uint4*>(kb + kKVChunk + sw128_offset(kr, u)) = w2[q];
                 }
             }
             // V needs no work here: pages without keys are not read (their rows
