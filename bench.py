@@ -70,10 +70,10 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    # decode call = decode_shared 4,635,946,325 + 72,088,917; combine 70,300,501 + 4,011;
-    # append 297,557 (read + write bytes, mean of three calls); prefill 8,636,470,272 + 260,794,880
-    ("llama3_70b", "decode"): (4778637312.0, "4b0fef217048ee08"),
-    ("llama3_70b", "prefill"): (8897265152.0, "4003343b0cf0199c"),
+    # decode call = decode_shared 4,636,219,392 + 72,291,584; combine 70,303,573 + 19,541;
+    # append 297,643 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
+    ("llama3_70b", "decode"): (4779131733.0, "c8345d8980f87c64"),
+    ("llama3_70b", "prefill"): (8812061184.0, "176d1c203b16d929"),
 }
 
 
