@@ -567,6 +567,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool reader = j < n_users;
         PlanUser us = {0, 0, 0, 0};
         if (reader) us = P.users[unit.user0 + j];
+        const __nv_bfloat16* qp_ = P.q + ((size_t)us.request * Hq + (size_t)h * g + head) * kD;
+        // The reader's q row (written before this call, not by the append) is
+        // fetched into L1 while the append finishes.
+        if (reader) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(qp_));
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(qp_ + 64));
+        }
         grid_dep_wait();   // the append's positions (and, for the tail run, its keys)
         const int m = reader ? P.qpos[us.request] : -1;
         const int pos_q = PREROT ? m : m - us.delta;   // the row's position relative to the run
@@ -580,8 +587,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (row_valid) {
             uint8_t* qsm = sm + kOffQ;
             const float sc = kLog2e * pv.qk_scale;
-            const __nv_bfloat16* qp_ = P.q + ((size_t)us.request * Hq + (size_t)h * g + head) * kD;
             const float* csq = reinterpret_cast<const float*>(pv.rope + (size_t)pos_q * (kD / 2));
+            if (!ALIBI) {   // the row's position-table line (512 B) into L1 beside the q words
+#pragma unroll
+                for (int l = 0; l < 4; ++l) asm volatile("prefetch.global.L1 [%0];" ::"l"(csq + 32 * l));
+            }
             float n2 = 0.f;   // input range: rotated, scaled pairs must stay finite in fp16
 #pragma unroll 2
             for (int uu = 0; uu < 8; ++uu) {
