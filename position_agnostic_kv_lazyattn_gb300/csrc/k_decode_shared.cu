@@ -780,45 +780,76 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // One CTA per (KV head, request): merge the request's partial results. Thread
-// = (query head hh of the group, 8 dims). Launched as a programmatic dependent
-// of the units' kernel; waits for it before reading the partials.
-__global__ void __launch_bounds__(128)
+// = (part, query head hh of the group, 8 dims): each of the four parts merges
+// every fourth partial in one pass (running maximum, its sum and output
+// rescaled when it grows), then part 0 merges the four through shared memory.
+// Launched as a programmatic dependent of the units' kernel; waits for it
+// before reading the partials.
+constexpr int kCombineParts = 4;
+__global__ void __launch_bounds__(128 * kCombineParts)
     decode_combine_kernel(PoolView pv, const int32_t* pbase, const int32_t* qpos, const float2* ml, const float* acc,
                           __nv_bfloat16* out, int g) {
+    __shared__ float s_m[kCombineParts][128], s_l[kCombineParts][128];
+    __shared__ float4 s_a[kCombineParts][2][128];
     grid_dep_launch_dependents();
     grid_dep_wait();
-    const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
-    const int hh = tid >> 4, d0 = (tid & 15) * 8;
-    if (hh >= g) return;
+    const int h = blockIdx.x, r = blockIdx.y;
+    const int part = threadIdx.x >> 7, t = threadIdx.x & 127;
+    const int hh = t >> 4, d0 = (t & 15) * 8;
     const int Hkv = pv.hkv;
-    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)r * pv.hq + (size_t)h * g + hh) * kD + d0);
+    const bool row = hh < g;
     const int k0 = pbase[r], k1 = pbase[r + 1];
-    float M = -INFINITY;
-    if (qpos[r] >= 0)
-        for (int k = k0; k < k1; ++k) {
-            const float2 x = __ldcg(&ml[((size_t)k * Hkv + h) * g + hh]);
-            if (x.y > 0.f) M = fmaxf(M, x.x);
-        }
-    float L = 0.f, a[8];
+    float M = -INFINITY, L = 0.f, a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = 0.f;
-    if (M != -INFINITY) {
+    if (row && qpos[r] >= 0) {
 #pragma unroll 4
-        for (int k = k0; k < k1; ++k) {
+        for (int k = k0 + part; k < k1; k += kCombineParts) {
             const size_t slot = ((size_t)k * Hkv + h) * g + hh;
             const float2 x = __ldcg(&ml[slot]);
-            if (!(x.y > 0.f)) continue;
-            const float w = fast_exp2(x.x - M);
-            L += x.y * w;
             const float4* src = reinterpret_cast<const float4*>(acc + slot * kD + d0);
             const float4 s0 = __ldcg(src), s1 = __ldcg(src + 1);
+            if (!(x.y > 0.f)) continue;   // a partial without keys
+            if (x.x > M) {                // new reference: earlier terms scaled down (0 from -inf)
+                const float sc = fast_exp2(M - x.x);
+                L *= sc;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[i] *= sc;
+                M = x.x;
+            }
+            const float w = fast_exp2(x.x - M);
+            L += x.y * w;
             a[0] += s0.x * w; a[1] += s0.y * w; a[2] += s0.z * w; a[3] += s0.w * w;
             a[4] += s1.x * w; a[5] += s1.y * w; a[6] += s1.z * w; a[7] += s1.w * w;
         }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    *dst = make_uint4(pack_bf2(a[0] * inv, a[1] * inv), pack_bf2(a[2] * inv, a[3] * inv),
-                      pack_bf2(a[4] * inv, a[5] * inv), pack_bf2(a[6] * inv, a[7] * inv));
+    s_m[part][t] = M;
+    s_l[part][t] = L;
+    s_a[part][0][t] = make_float4(a[0], a[1], a[2], a[3]);
+    s_a[part][1][t] = make_float4(a[4], a[5], a[6], a[7]);
+    __syncthreads();
+    if (part != 0 || !row) return;
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kCombineParts; ++q) Mx = fmaxf(Mx, s_m[q][t]);
+    float Ls = 0.f, o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    if (Mx != -INFINITY) {
+#pragma unroll
+        for (int q = 0; q < kCombineParts; ++q) {
+            if (!(s_l[q][t] > 0.f)) continue;
+            const float w = fast_exp2(s_m[q][t] - Mx);
+            Ls += s_l[q][t] * w;
+            const float4 u0 = s_a[q][0][t], u1 = s_a[q][1][t];
+            o[0] += u0.x * w; o[1] += u0.y * w; o[2] += u0.z * w; o[3] += u0.w * w;
+            o[4] += u1.x * w; o[5] += u1.y * w; o[6] += u1.z * w; o[7] += u1.w * w;
+        }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)r * pv.hq + (size_t)h * g + hh) * kD + d0);
+    *dst = make_uint4(pack_bf2(o[0] * inv, o[1] * inv), pack_bf2(o[2] * inv, o[3] * inv),
+                      pack_bf2(o[4] * inv, o[5] * inv), pack_bf2(o[6] * inv, o[7] * inv));
 }
 
 using SharedKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
@@ -888,7 +919,7 @@ int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const 
             return LAZYATTN_ECUDA;
     }
     const int32_t* pbase = reinterpret_cast<const int32_t*>(img + plan.pbase_off);
-    if (launch_dependent(decode_combine_kernel, dim3(p.d.n_kv_heads, b.num_requests), dim3(128), 0, stream, p.view(),
+    if (launch_dependent(decode_combine_kernel, dim3(p.d.n_kv_heads, b.num_requests), dim3(128 * kCombineParts), 0, stream, p.view(),
                          pbase, P.qpos, static_cast<const float2*>(P.ml), static_cast<const float*>(P.acc), out,
                          P.g) != cudaSuccess)
         return LAZYATTN_ECUDA;
