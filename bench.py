@@ -70,9 +70,9 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    # decode call = decode_shared 4,636,299,008 + 72,167,765; combine 70,301,269 + 23,210;
-    # append 298,154 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
-    ("llama3_70b", "decode"): (4779089408.0, "b2452744e1acaac3"),
+    # decode call = decode_shared 4,636,025,685 + 72,102,485; combine 70,299,050 + 25,173;
+    # append 298,155 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
+    ("llama3_70b", "decode"): (4778750549.0, "3b48bb60bdcd611f"),
     ("llama3_70b", "prefill"): (8812061184.0, "176d1c203b16d929"),
 }
 
