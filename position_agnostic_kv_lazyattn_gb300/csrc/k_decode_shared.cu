@@ -189,10 +189,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = P.g, Hq = pv.hq, Hkv = pv.hkv;
-    const PlanUnit unit = P.units[blockIdx.x];   // the plan is not written by the append
+    // CTA = (unit, KV head) with the KV head fastest: the CTAs that run together
+    // read whole pages ([page][Hkv][16][D]), and the shortest units of every
+    // head come last
+    const int h = (int)(blockIdx.x % (unsigned)Hkv);
+    const PlanUnit unit = P.units[blockIdx.x / (unsigned)Hkv];   // the plan is not written by the append
     const bool priv = (unit.n_users & kUnitPrivate) != 0;
     const int n_users = unit.n_users & ~kUnitPrivate;
     const int np = unit.n_pages;
@@ -913,7 +916,7 @@ int launch_decode_shared(const lazyattn_pool& p, const lazyattn_batch& b, const 
     auto kern = shared_kernel_for((b.flags & LAZYATTN_KEYS_PREROTATED) != 0, p.d.key_storage == LAZYATTN_KEYS_DOC_LOCAL,
                                   p.d.rope_interleaved != 0, p.d.position_encoding == LAZYATTN_POS_ALIBI);
     if (plan.num_units > 0) {
-        dim3 grid(plan.num_units, p.d.n_kv_heads);
+        dim3 grid(plan.num_units * p.d.n_kv_heads);
         if (launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, stream, p.kmap, p.vmap, p.kmap4, p.vmap4, p.rmap4,
                              p.view(), P) != cudaSuccess)
             return LAZYATTN_ECUDA;
