@@ -13,8 +13,9 @@
 // position n = delta + t. §3.2 "Decoding" (rotate q, not K, per document) is
 // the same move for the paper's own doc-local layout.
 //
-// CTA = (unit u, KV head h), two per SM: up to 128 query rows, one per
-// (reader, query head of the group), at TMEM lane reader * g + head. Tiles of
+// CTA = (unit u, KV head h), launched with the KV head fastest, two per SM:
+// up to 128 query rows, one per (reader, query head of the group), at TMEM
+// lane reader * g + head. Tiles of
 // 64 keys (4 pages) stream through two-stage K and V rings. Roles (12 warps):
 //   warp 0        TMA producer of K: the unit's entries (read by the whole
 //                 warp in one round trip), each page's position-table row for
