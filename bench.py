@@ -70,9 +70,9 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    # decode call = decode_shared 4,636,025,685 + 72,102,485; combine 70,299,050 + 25,173;
-    # append 298,155 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
-    ("llama3_70b", "decode"): (4778750549.0, "3b48bb60bdcd611f"),
+    # decode call = decode_shared 4,638,789,973 + 71,077,546; combine 70,299,562 + 18,517;
+    # append 298,069 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
+    ("llama3_70b", "decode"): (4780483669.0, "b95726e7c2b8f11d"),
     ("llama3_70b", "prefill"): (8812061184.0, "176d1c203b16d929"),
 }
 
