@@ -790,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Launched as a programmatic dependent of the units' kernel; waits for it
 // before reading the partials.
 constexpr int kCombineParts = 4;
-__global__ void __launch_bounds__(128 * kCombineParts)
+// (at most 32 registers: four CTAs per SM, so 148 SMs hold 592 of them in one wave)
+__global__ void __launch_bounds__(128 * kCombineParts, 4)
     decode_combine_kernel(PoolView pv, const int32_t* pbase, const int32_t* qpos, const float2* ml, const float* acc,
                           __nv_bfloat16* out, int g) {
     __shared__ float s_m[kCombineParts][128], s_l[kCombineParts][128];
