@@ -70,9 +70,9 @@ ROPE_PRESETS = {
 }
 
 NCU_TRAFFIC = {
-    # decode call = decode_shared 4,638,789,973 + 71,077,546; combine 70,299,562 + 18,517;
-    # append 298,069 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
-    ("llama3_70b", "decode"): (4780483669.0, "b95726e7c2b8f11d"),
+    # decode call = decode_shared 4,638,851,242 + 71,246,848; combine 70,299,648 + 40,106;
+    # append 297,984 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
+    ("llama3_70b", "decode"): (4780735829.0, "2a1c10fcf6f24cae"),
     ("llama3_70b", "prefill"): (8812061184.0, "176d1c203b16d929"),
 }
 
