@@ -72,7 +72,7 @@ ROPE_PRESETS = {
 NCU_TRAFFIC = {
     # decode call = decode_shared 4,638,851,242 + 71,246,848; combine 70,299,648 + 40,106;
     # append 297,984 (read + write bytes, mean of three calls); prefill 8,550,291,968 + 261,769,216
-    ("llama3_70b", "decode"): (4780735829.0, "2a1c10fcf6f24cae"),
+    ("llama3_70b", "decode"): (4780735829.0, "4f7db189cf4decee"),
     ("llama3_70b", "prefill"): (8812061184.0, "176d1c203b16d929"),
 }
 

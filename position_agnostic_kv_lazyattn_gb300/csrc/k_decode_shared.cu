@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Launched as a programmatic dependent of the units' kernel; waits for it
 // before reading the partials.
 constexpr int kCombineParts = 4;
-// (at most 32 registers: four CTAs per SM, so 148 SMs hold 592 of them in one wave)
+// (at most 32 registers: four CTAs per SM, so the 152 SMs hold 608 of them in one wave)
 __global__ void __launch_bounds__(128 * kCombineParts, 4)
     decode_combine_kernel(PoolView pv, const int32_t* pbase, const int32_t* qpos, const float2* ml, const float* acc,
                           __nv_bfloat16* out, int g) {
